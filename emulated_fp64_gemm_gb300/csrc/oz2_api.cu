@@ -1,0 +1,588 @@
+// C ABI of the Ozaki-II FP64 GEMM: argument checks, host-side constants,
+// the library-owned workspace and the launch sequence of the pipeline
+// ("Profiling Ozaki II: The Cost Behind Fast INT8 GEMMs" §1 pipeline table;
+// "Ozaki II supplement: INT8 range conditions and paper performance results"
+// §1.1-§1.3 for the moduli, residue range and INT32 condition).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "oz2_internal.cuh"
+
+namespace oz2 {
+namespace {
+
+// ------------------------------------------------------------ small big-integers
+constexpr int kBigLimbs = 6;
+struct Big {
+  uint32_t l[kBigLimbs] = {0, 0, 0, 0, 0, 0};
+};
+
+void big_mul_small(Big& a, uint32_t m) {
+  uint64_t c = 0;
+  for (int k = 0; k < kBigLimbs; ++k) {
+    const uint64_t t = static_cast<uint64_t>(a.l[k]) * m + c;
+    a.l[k] = static_cast<uint32_t>(t);
+    c = t >> 32;
+  }
+}
+
+uint32_t big_divmod_small(Big& a, uint32_t m) {  // a /= m, returns a mod m
+  uint64_t rem = 0;
+  for (int k = kBigLimbs - 1; k >= 0; --k) {
+    const uint64_t cur = (rem << 32) | a.l[k];
+    a.l[k] = static_cast<uint32_t>(cur / m);
+    rem = cur % m;
+  }
+  return static_cast<uint32_t>(rem);
+}
+
+int big_bitlen(const Big& a) {
+  for (int k = kBigLimbs - 1; k >= 0; --k)
+    if (a.l[k]) {
+      int b = 0;
+      while ((a.l[k] >> b) != 0) ++b;
+      return 32 * k + b;
+    }
+  return 0;
+}
+
+bool big_bit(const Big& a, int pos) { return (a.l[pos >> 5] >> (pos & 31)) & 1u; }
+
+int gcd(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+struct Tables {
+  int moduli[kSMax];
+  HostConsts hc[kSMax + 1];
+  std::vector<uint8_t> pow2mod;  // [kSMax][kPow2Max]
+};
+
+const Tables& tables() {
+  static Tables T;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    // greedy: walk down from 256, keep each integer coprime to all kept
+    int n = 0;
+    for (int m = 256; m >= 2 && n < kSMax; --m) {
+      bool ok = true;
+      for (int k = 0; k < n; ++k) ok = ok && gcd(m, T.moduli[k]) == 1;
+      if (ok) T.moduli[n++] = m;
+    }
+    T.pow2mod.assign(static_cast<size_t>(kSMax) * kPow2Max, 0);
+    for (int t = 0; t < kSMax; ++t) {
+      uint32_t v = 1 % T.moduli[t];
+      for (int k = 0; k < kPow2Max; ++k) {
+        T.pow2mod[static_cast<size_t>(t) * kPow2Max + k] = static_cast<uint8_t>(v);
+        v = (v * 2) % T.moduli[t];
+      }
+    }
+    for (int s = OZ2_S_MIN; s <= kSMax; ++s) {
+      HostConsts& h = T.hc[s];
+      std::memset(&h, 0, sizeof(h));
+      ModConsts& mc = h.mod;
+      CrtConsts& cc = h.crt;
+      mc.s = s;
+      cc.s = s;
+      Big M;
+      M.l[0] = 1;
+      for (int t = 0; t < s; ++t) big_mul_small(M, static_cast<uint32_t>(T.moduli[t]));
+      for (int t = 0; t < s; ++t) {
+        const uint32_t m = static_cast<uint32_t>(T.moduli[t]);
+        mc.m[t] = static_cast<int>(m);
+        mc.half[t] = static_cast<int>(m / 2);
+        mc.magic39[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
+        mc.magic32[t] = static_cast<uint32_t>(((1ull << 32) + m - 1) / m);
+        for (int k = 0; k < 3; ++k) {
+          uint64_t w = 1;
+          for (int b = 0; b < 21 * k; ++b) w = (w * 2) % m;
+          mc.w21[t][k] = static_cast<uint32_t>(w);
+        }
+        for (int k = 0; k < 4; ++k) {
+          uint64_t w = 1;
+          for (int b = 0; b < 20 * k; ++b) w = (w * 2) % m;
+          mc.w20[t][k] = static_cast<uint32_t>(w);
+        }
+        mc.KH[t] = static_cast<uint32_t>(m * (((1u << 30) + m - 1) / m) + m / 2);
+        mc.mf[t] = static_cast<float>(m);
+        mc.inv_mf[t] = 1.0f / static_cast<float>(m);
+        // CRT constants
+        cc.m[t] = static_cast<int>(m);
+        cc.magic32[t] = mc.magic32[t];
+        Big Mt = M;
+        const uint32_t rem = big_divmod_small(Mt, m);
+        (void)rem;  // M is a multiple of m
+        for (int k = 0; k < kLimbs; ++k) cc.Mt[t][k] = Mt.l[k];
+        Big tmp = Mt;
+        const uint32_t mt_mod = big_divmod_small(tmp, m);
+        uint32_t inv = 0;
+        for (uint32_t x = 1; x < m; ++x)
+          if ((static_cast<uint64_t>(mt_mod) * x) % m == 1) {
+            inv = x;
+            break;
+          }
+        cc.inv[t] = inv;
+      }
+      for (int k = 0; k < kLimbs; ++k) cc.M[k] = M.l[k];
+      Big Mh = M;
+      big_divmod_small(Mh, 2);
+      for (int k = 0; k < kLimbs; ++k) cc.Mhalf[k] = Mh.l[k];
+      int top = 0;
+      for (int k = kLimbs - 1; k >= 0; --k)
+        if (M.l[k]) {
+          top = k;
+          break;
+        }
+      if (top < 1) top = 1;
+      cc.top = top;
+      const double mtop = static_cast<double>(M.l[top]) * 4294967296.0 + static_cast<double>(M.l[top - 1]);
+      cc.inv_Mtop = static_cast<float>(1.0 / mtop);
+      // L = M/2 - 1
+      Big L = Mh;
+      for (int k = 0; k < kBigLimbs; ++k) {  // subtract 1
+        if (L.l[k] != 0) {
+          L.l[k] -= 1;
+          break;
+        }
+        L.l[k] = 0xFFFFFFFFu;
+      }
+      const int lb = big_bitlen(L);
+      h.bound.Lbits = lb;
+      uint64_t norm = 0;
+      for (int b = 0; b < 64; ++b) {
+        const int pos = lb - 1 - b;
+        norm <<= 1;
+        if (pos >= 0 && big_bit(L, pos)) norm |= 1;
+      }
+      h.bound.Lnorm = norm;
+    }
+  });
+  return T;
+}
+
+// ------------------------------------------------------------ per-device state
+struct DeviceState {
+  int* err = nullptr;          // device error word
+  uint8_t* pow2mod = nullptr;  // [kSMax][kPow2Max]
+  int num_sms = 0;
+  bool supported = false;
+};
+
+struct Workspace {
+  size_t bytes = 0;
+  uint8_t* base = nullptr;
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceState> g_dev;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+oz2_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZ2_ERR_CUDA;
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DeviceState ds;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    ds.supported = (major == 10 && minor == 3);
+    if (ds.supported) {
+      if (cudaMalloc(&ds.err, sizeof(int)) != cudaSuccess) return OZ2_ERR_NO_MEMORY;
+      if (cudaMemset(ds.err, 0, sizeof(int)) != cudaSuccess) return OZ2_ERR_CUDA;
+      const auto& T = tables();
+      if (cudaMalloc(&ds.pow2mod, T.pow2mod.size()) != cudaSuccess) return OZ2_ERR_NO_MEMORY;
+      if (cudaMemcpy(ds.pow2mod, T.pow2mod.data(), T.pow2mod.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        return OZ2_ERR_CUDA;
+    }
+    it = g_dev.emplace(dev, ds).first;
+  }
+  *out = &it->second;
+  return it->second.supported ? OZ2_OK : OZ2_ERR_UNSUPPORTED_DEVICE;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t alpha, beta, amaxA, amaxB, sumA, sumB, u, v, rowkey, colkey, planesA, planesB, R;
+  size_t stageA, stageB, stageC;
+  size_t total;
+};
+
+Layout make_layout(int64_t p, int64_t q, int64_t r, int s, int64_t qp, bool staging) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.alpha = take(p * 4);
+  L.beta = take(r * 4);
+  L.amaxA = take(p * 8);
+  L.amaxB = take(r * 8);
+  L.sumA = take(p * 8);
+  L.sumB = take(r * 8);
+  L.u = take(p * 4);
+  L.v = take(r * 4);
+  L.rowkey = take(p * 8);
+  L.colkey = take(r * 8);
+  L.planesA = take(static_cast<size_t>(s) * p * qp * 2);
+  L.planesB = take(static_cast<size_t>(s) * r * qp * 2);
+  L.R = take(static_cast<size_t>(s) * p * r);
+  if (staging) {
+    L.stageA = take(static_cast<size_t>(p) * q * 8);
+    L.stageB = take(static_cast<size_t>(q) * r * 8);
+    L.stageC = take(static_cast<size_t>(p) * r * 8);
+  }
+  L.total = off;
+  (void)q;
+  return L;
+}
+
+oz2_status get_workspace(cudaStream_t st, size_t bytes, uint8_t** base) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZ2_ERR_CUDA;
+  Workspace& w = g_ws[std::make_pair(dev, st)];
+  if (w.bytes < bytes) {
+    if (w.base) {
+      cudaDeviceSynchronize();
+      cudaFree(w.base);
+      w.base = nullptr;
+      w.bytes = 0;
+    }
+    if (std::getenv("OZ2_FAIL_ALLOC") != nullptr) return OZ2_ERR_NO_MEMORY;  // host-side fault injection
+    if (cudaMalloc(&w.base, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      w.base = nullptr;
+      return OZ2_ERR_NO_MEMORY;
+    }
+    w.bytes = bytes;
+  }
+  *base = w.base;
+  return OZ2_OK;
+}
+
+oz2_status check_args(int64_t p, int64_t q, int64_t r, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, const void* C, int64_t ldc, int s, int mode) {
+  if (p <= 0 || q <= 0 || r <= 0) return OZ2_ERR_INVALID_ARG;
+  if (lda < p || ldb < q || ldc < p) return OZ2_ERR_INVALID_ARG;
+  if (!A || !B || !C) return OZ2_ERR_INVALID_ARG;
+  if (s < OZ2_S_MIN || s > OZ2_S_MAX) return OZ2_ERR_INVALID_ARG;
+  if (mode != OZ2_FAST && mode != OZ2_ACCU) return OZ2_ERR_INVALID_ARG;
+  if (q >= OZ2_Q_LIMIT) return OZ2_ERR_Q_TOO_LARGE;
+  if (p > (int64_t(1) << 31) - 1024 || r > (int64_t(1) << 31) - 1024) return OZ2_ERR_INVALID_ARG;
+  return OZ2_OK;
+}
+
+struct Outputs {  // optional checking outputs
+  int32_t* alpha = nullptr;
+  int32_t* beta = nullptr;
+  int8_t* Ares = nullptr;
+  int8_t* Bres = nullptr;
+  int32_t* P = nullptr;
+  uint8_t* R = nullptr;
+  uint64_t* X = nullptr;
+};
+
+#define OZ2_CU(call)                                 \
+  do {                                               \
+    if ((call) != cudaSuccess) return OZ2_ERR_CUDA;  \
+  } while (0)
+
+// The pipeline.  ev (optional, 6 events) is recorded at the stage boundaries.
+oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
+                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                        cudaStream_t st, const Outputs* dbg, cudaEvent_t* ev, uint8_t** ws_out,
+                        Layout* lay_out) {
+  DeviceState* ds = nullptr;
+  oz2_status e = device_state(&ds);
+  if (e != OZ2_OK) return e;
+  const HostConsts* hc = host_consts(s);
+  const int64_t qp = (q + kKPad - 1) / kKPad * kKPad;
+  const Layout L = make_layout(p, q, r, s, qp, lay_out != nullptr);
+  uint8_t* ws = nullptr;
+  e = get_workspace(st, L.total, &ws);
+  if (e != OZ2_OK) return e;
+  if (ws_out) *ws_out = ws;
+  if (lay_out) *lay_out = L;
+  auto at = [&](size_t off) { return ws + off; };
+  int32_t* alpha = reinterpret_cast<int32_t*>(at(L.alpha));
+  int32_t* beta = reinterpret_cast<int32_t*>(at(L.beta));
+  uint64_t* amaxA = reinterpret_cast<uint64_t*>(at(L.amaxA));
+  uint64_t* amaxB = reinterpret_cast<uint64_t*>(at(L.amaxB));
+  uint16_t* planesA = reinterpret_cast<uint16_t*>(at(L.planesA));
+  uint16_t* planesB = reinterpret_cast<uint16_t*>(at(L.planesB));
+  uint8_t* Rw = at(L.R);
+  ScaleArgs sa{p, q, r, lda, ldb, A, B};
+
+  if (ev) OZ2_CU(cudaEventRecord(ev[0], st));
+  if (mode == OZ2_FAST) {
+    OZ2_CU(launch_fast_exponents(sa, hc->bound, amaxA, amaxB, reinterpret_cast<uint64_t*>(at(L.sumA)),
+                                 reinterpret_cast<uint64_t*>(at(L.sumB)), alpha, beta, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
+  } else {
+    int32_t* u = reinterpret_cast<int32_t*>(at(L.u));
+    int32_t* v = reinterpret_cast<int32_t*>(at(L.v));
+    uint64_t* rowkey = reinterpret_cast<uint64_t*>(at(L.rowkey));
+    uint64_t* colkey = reinterpret_cast<uint64_t*>(at(L.colkey));
+    // the bound planes live in the first plane of each residue buffer: they
+    // are consumed by the bound GEMM before the residue kernels overwrite them
+    uint16_t* Abar = planesA;
+    uint16_t* Bbar = planesB;
+    OZ2_CU(launch_bound_quant(sa, qp, amaxA, amaxB, u, v, Abar, Bbar, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
+    OZ2_CU(cudaMemsetAsync(rowkey, 0, p * 8, st));
+    OZ2_CU(cudaMemsetAsync(colkey, 0, r * 8, st));
+    GemmArgs g{};
+    g.p = p;
+    g.r = r;
+    g.qp = qp;
+    g.s = 1;
+    g.Aplanes = Abar;
+    g.Bplanes = Bbar;
+    g.rowkey = rowkey;
+    g.colkey = colkey;
+    g.u = u;
+    g.v = v;
+    g.err = ds->err;
+    g.num_sms = ds->num_sms;
+    OZ2_CU(launch_gemm(kGemmBound, g, hc->mod, st));
+    OZ2_CU(launch_accu_exponents(p, r, hc->bound, rowkey, colkey, u, v, alpha, beta, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
+  }
+  // |trunc(2^alpha a)| <= sqrt(L) in fast mode; accu entries beyond the limbs take the general path
+  const int max_bits = (hc->bound.Lbits + 1) / 2;
+  OZ2_CU(launch_residues(sa, qp, hc->mod, alpha, beta, ds->pow2mod, max_bits, max_bits, planesA,
+                         planesB, st));
+  if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
+  {
+    GemmArgs g{};
+    g.p = p;
+    g.r = r;
+    g.qp = qp;
+    g.s = s;
+    g.Aplanes = planesA;
+    g.Bplanes = planesB;
+    g.R = Rw;
+    g.err = ds->err;
+    g.num_sms = ds->num_sms;
+    OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
+  }
+  if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
+  OZ2_CU(launch_crt(p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
+  if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
+
+  if (dbg) {
+    if (dbg->alpha) OZ2_CU(cudaMemcpyAsync(dbg->alpha, alpha, p * 4, cudaMemcpyDeviceToDevice, st));
+    if (dbg->beta) OZ2_CU(cudaMemcpyAsync(dbg->beta, beta, r * 4, cudaMemcpyDeviceToDevice, st));
+    if (dbg->R) OZ2_CU(cudaMemcpyAsync(dbg->R, Rw, static_cast<size_t>(s) * p * r, cudaMemcpyDeviceToDevice, st));
+    if (dbg->Ares) OZ2_CU(launch_planes_to_int8(planesA, p, q, qp, s, dbg->Ares, st));
+    if (dbg->Bres) OZ2_CU(launch_planes_to_int8(planesB, r, q, qp, s, dbg->Bres, st));
+    if (dbg->P) {
+      GemmArgs g{};
+      g.p = p;
+      g.r = r;
+      g.qp = qp;
+      g.s = s;
+      g.Aplanes = planesA;
+      g.Bplanes = planesB;
+      g.P = dbg->P;
+      g.err = ds->err;
+      g.num_sms = ds->num_sms;
+      OZ2_CU(launch_gemm(kGemmExactP, g, hc->mod, st));
+    }
+  }
+  return OZ2_OK;
+}
+
+}  // namespace
+
+const HostConsts* host_consts(int s) {
+  if (s < OZ2_S_MIN || s > kSMax) return nullptr;
+  return &tables().hc[s];
+}
+
+const int* greedy_moduli20() { return tables().moduli; }
+
+}  // namespace oz2
+
+// =================================================================== C ABI
+using namespace oz2;
+
+extern "C" {
+
+oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
+                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                        void* stream) {
+  oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
+  if (e != OZ2_OK) return e;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, static_cast<cudaStream_t>(stream),
+                      nullptr, nullptr, nullptr, nullptr);
+}
+
+oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
+                              const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                              void* stream, int32_t* alpha, int32_t* beta, int8_t* Ares,
+                              int8_t* Bres, int32_t* P, uint8_t* R, uint64_t* X) {
+  oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
+  if (e != OZ2_OK) return e;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  Outputs o;
+  o.alpha = alpha;
+  o.beta = beta;
+  o.Ares = Ares;
+  o.Bres = Bres;
+  o.P = P;
+  o.R = R;
+  o.X = X;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, &o, nullptr, nullptr, nullptr);
+  if (e != OZ2_OK) return e;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return OZ2_ERR_CUDA;
+  return OZ2_OK;
+}
+
+oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
+                               const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                               void* stream, float* stage_ms) {
+  oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
+  if (e != OZ2_OK) return e;
+  if (!stage_ms) return OZ2_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t ev[6];
+  for (auto& x : ev)
+    if (cudaEventCreate(&x) != cudaSuccess) return OZ2_ERR_CUDA;
+  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, nullptr, ev, nullptr, nullptr);
+  if (e == OZ2_OK) {
+    if (cudaEventSynchronize(ev[5]) != cudaSuccess) e = OZ2_ERR_CUDA;
+    for (int k = 0; k < 5 && e == OZ2_OK; ++k) cudaEventElapsedTime(&stage_ms[k], ev[k], ev[k + 1]);
+    if (e == OZ2_OK) cudaEventElapsedTime(&stage_ms[5], ev[0], ev[5]);
+  }
+  for (auto& x : ev) cudaEventDestroy(x);
+  return e;
+}
+
+oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
+                             const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                             void* stream) {
+  oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
+  if (e != OZ2_OK) return e;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceState* ds = nullptr;
+  e = device_state(&ds);
+  if (e != OZ2_OK) return e;
+  const int64_t qp = (q + kKPad - 1) / kKPad * kKPad;
+  const Layout L = make_layout(p, q, r, s, qp, true);
+  uint8_t* ws = nullptr;
+  e = get_workspace(st, L.total, &ws);
+  if (e != OZ2_OK) return e;
+  double* dA = reinterpret_cast<double*>(ws + L.stageA);
+  double* dB = reinterpret_cast<double*>(ws + L.stageB);
+  double* dC = reinterpret_cast<double*>(ws + L.stageC);
+  OZ2_CU(cudaMemcpy2DAsync(dA, p * 8, A, lda * 8, p * 8, q, cudaMemcpyHostToDevice, st));
+  OZ2_CU(cudaMemcpy2DAsync(dB, q * 8, B, ldb * 8, q * 8, r, cudaMemcpyHostToDevice, st));
+  Layout L2;
+  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2);
+  if (e != OZ2_OK) return e;
+  OZ2_CU(cudaMemcpy2DAsync(C, ldc * 8, dC, p * 8, p * 8, r, cudaMemcpyDeviceToHost, st));
+  OZ2_CU(cudaStreamSynchronize(st));
+  return OZ2_OK;
+}
+
+int ozaki2_moduli(int s, int32_t* out) {
+  if (s < OZ2_S_MIN || s > OZ2_S_MAX || !out) return -1;
+  const int* m = greedy_moduli20();
+  for (int t = 0; t < s; ++t) out[t] = m[t];
+  return s;
+}
+
+oz2_status ozaki2_last_error(void) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  oz2_status res = OZ2_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_dev) {
+    if (!kv.second.err) continue;
+    cudaSetDevice(kv.first);
+    int v = 0;
+    if (cudaMemcpy(&v, kv.second.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      res = OZ2_ERR_CUDA;
+      continue;
+    }
+    if (v & kErrTimeout) {
+      res = OZ2_ERR_DEVICE_TIMEOUT;
+      cudaMemset(kv.second.err, 0, sizeof(int));
+    }
+  }
+  cudaSetDevice(cur);
+  return res;
+}
+
+void ozaki2_workspace_release(void) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    if (kv.second.base) {
+      cudaSetDevice(kv.first.first);
+      cudaDeviceSynchronize();
+      cudaFree(kv.second.base);
+    }
+  }
+  g_ws.clear();
+  cudaSetDevice(cur);
+}
+
+const char* ozaki2_status_string(oz2_status status) {
+  switch (status) {
+    case OZ2_OK: return "ok";
+    case OZ2_ERR_INVALID_ARG: return "invalid argument";
+    case OZ2_ERR_Q_TOO_LARGE: return "inner dimension q >= 131072";
+    case OZ2_ERR_NO_MEMORY: return "workspace allocation failed";
+    case OZ2_ERR_CUDA: return "CUDA error";
+    case OZ2_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case OZ2_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+  }
+  return "unknown status";
+}
+
+oz2_status ozaki2_selftest_wait_timeout(int limit_us) {
+  if (limit_us < 1 || limit_us > 1000000) return OZ2_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceState* ds = nullptr;
+  oz2_status e = device_state(&ds);
+  if (e != OZ2_OK) return e;
+  int* err = nullptr;
+  if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return OZ2_ERR_NO_MEMORY;
+  cudaMemset(err, 0, sizeof(int));
+  if (launch_wait_timeout_selftest(err, static_cast<long long>(limit_us) * 1000, nullptr) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(err);
+    return OZ2_ERR_CUDA;
+  }
+  int v = 0;
+  cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(err);
+  return (v & kErrTimeout) ? OZ2_ERR_DEVICE_TIMEOUT : OZ2_OK;
+}
+
+}  // extern "C"

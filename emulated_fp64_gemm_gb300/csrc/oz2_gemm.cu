@@ -1,0 +1,567 @@
+// The s modular GEMMs P_t = A_t B_t of Ozaki II on the 5th-generation tensor
+// cores (tcgen05), with the output reduction R_t = P_t mod m_t fused into the
+// epilogue ("Profiling Ozaki II: The Cost Behind Fast INT8 GEMMs" §1, yellow
+// and blue stages; "Ozaki II supplement ..." §1.3 for the exactness condition).
+//
+// sm_103a has no integer tcgen05 MMA, so the residues (integers in
+// [-128, 127]) are carried exactly as fp16 and multiplied with
+// tcgen05.mma.kind::f16 into fp32 accumulators in tensor memory.  Every
+// product is an integer of magnitude <= 2^14 and every partial sum stays an
+// integer below 2^24 in magnitude, so the fp32 accumulation is exact as long
+// as a K-chunk holds at most 960 terms:
+//   * kGemmMod (the production path): after each K-chunk the epilogue warps
+//     replace every accumulator D by D - m*rint(D/m), an exact fp32
+//     operation leaving |D| <= 129, and the next chunk accumulates on top.
+//     This is the supplement's §1.3 K-blocking (reduce each block modulo the
+//     modulus, then combine) done in tensor memory; it also frees the inner
+//     dimension from the INT32 bound.  The last chunk yields R_t = D mod m_t.
+//   * kGemmExactP / kGemmBound: each chunk starts from zero and is drained
+//     into an int32 running sum kept in tensor memory beside the
+//     accumulator, giving the exact P_t (checking path) or the exact bound
+//     product Wbar = Abar Bbar (accu mode), whose epilogue reduces every row
+//     and column to its maximum scaled value.
+//
+// Structure: one persistent CTA per SM, 6 warps.  Warp 0 issues TMA loads of
+// 128x64 (A) and BNx64 (B) fp16 tiles (128-byte swizzle) into a ring of
+// shared-memory stages; warp 1 allocates 512 TMEM columns and one thread of
+// it issues the MMAs; warps 2-5 are the epilogue.  A work unit is a pair of
+// output tiles (same rows, adjacent column tiles) of one channel t; the two
+// tiles own TMEM slots 0 and 1 and their K-chunks are interleaved, so while
+// the tensor core works on one tile the epilogue processes the other.
+// Every wait is bounded in time; a timeout sets the device error word and
+// the kernel winds down instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "oz2_internal.cuh"
+
+namespace oz2 {
+namespace {
+
+constexpr int BM = 128;           // tile rows (TMEM lanes)
+constexpr int BK = 64;            // K per stage: 64 fp16 = one 128-byte swizzle row
+constexpr int KC_BLOCKS = 15;     // K-chunk = 15 * 64 = 960 terms (< 2^24 / 2^14 - margin)
+constexpr int NUM_THREADS = 192;  // 6 warps
+constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256;
+};
+
+struct KParams {
+  int64_t p, r;
+  int s;
+  int nkb;          // K blocks (qp / 64)
+  int nchunks;      // ceil(nkb / KC_BLOCKS)
+  int tiles_m, tiles_n, pairs_n;
+  int64_t units;    // s * tiles_m * pairs_n
+  uint8_t* R;
+  int32_t* P;
+  uint64_t* rowkey;
+  uint64_t* colkey;
+  const int32_t* u;
+  const int32_t* v;
+  int* err;
+  float mf[kSMax];
+  float inv_mf[kSMax];
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused for SW128 K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;             // version
+  d |= static_cast<uint64_t>(2) << 61;             // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major.
+template <int BN>
+__device__ __forceinline__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+#define OZ2_REG32(v)                                                                          \
+  "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),        \
+      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), \
+      "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),           \
+      "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),           \
+      "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+#define OZ2_IREG32(v)                                                                          \
+  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),      \
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),        \
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),      \
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),      \
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+
+// 32 lanes x 32 consecutive 32-bit columns: thread = lane = tile row.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : OZ2_REG32(v)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      OZ2_IREG32(v)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Order-preserving key of the dyadic value w * 2^-x (w >= 0, w < 2^31).
+__device__ __forceinline__ uint64_t dyadic_key(uint32_t w, int x) {
+  if (w == 0) return 0;
+  const int b = 32 - __clz(static_cast<int>(w));  // bit length
+  const int E = b - 1 - x;                         // floor(log2 value)
+  return (static_cast<uint64_t>(E + 4096) << 32) | static_cast<uint64_t>(w << (32 - b));
+}
+
+// --------------------------------------------------------------------- unit decode
+struct Unit {
+  int t, tm, tn0, ntile;
+};
+
+__device__ __forceinline__ Unit decode_unit(int64_t u, const KParams& kp) {
+  const int64_t upp = static_cast<int64_t>(kp.tiles_m) * kp.pairs_n;
+  Unit U;
+  U.t = static_cast<int>(u / upp);
+  const int64_t w = u % upp;
+  // grouped raster: groups of GM row tiles, column pairs outer within a group
+  constexpr int GM = 8;
+  const int64_t per_group = static_cast<int64_t>(GM) * kp.pairs_n;
+  const int64_t g = w / per_group;
+  const int64_t idx = w % per_group;
+  const int64_t left = kp.tiles_m - g * GM;
+  const int rows_in_group = static_cast<int>(left < GM ? left : GM);
+  U.tm = static_cast<int>(g * GM + idx % rows_in_group);
+  const int pn = static_cast<int>(idx / rows_in_group);
+  U.tn0 = pn * 2;
+  U.ntile = (U.tn0 + 1 < kp.tiles_n) ? 2 : 1;
+  return U;
+}
+
+// --------------------------------------------------------------------- the kernel
+template <int BN, int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    oz2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ KParams kp) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;                     // [STAGES]
+  uint64_t* empty = bars + C::STAGES;        // [STAGES]
+  uint64_t* accf = bars + 2 * C::STAGES;     // [2]
+  uint64_t* acce = accf + 2;                 // [2]
+  uint64_t* drain = acce + 2;                // [1] final wait for in-flight MMAs on abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* issued_ctr = reinterpret_cast<int*>(tmem_slot + 2);
+  int* consumed_ctr = issued_ctr + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&accf[i]), 1);
+      mbar_init(smem_u32(&acce[i]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *issued_ctr = 0;
+    *consumed_ctr = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(u, kp);
+        for (int c = 0; c < kp.nchunks && ok; ++c) {
+          const int kb0 = c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, kp.nkb);
+          for (int sl = 0; sl < U.ntile && ok; ++sl) {
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb = smem_u32(&full[stage]);
+              mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+              tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK, U.tm * BM, U.t, fb);
+              tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK, (U.tn0 + sl) * BN, U.t, fb);
+              ++issued;
+              if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(kp.err, kErrTimeout);
+      }
+      *issued_ctr = issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc<BN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t use[2] = {0, 0};
+      int consumed = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(u, kp);
+        for (int c = 0; c < kp.nchunks && ok; ++c) {
+          const int kb0 = c * KC_BLOCKS;
+          const int kb1 = min(kb0 + KC_BLOCKS, kp.nkb);
+          for (int sl = 0; sl < U.ntile && ok; ++sl) {
+            if (!mbar_wait_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ++use[sl];
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(sl * 256);
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+              const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                const bool first = (kb == kb0) && (k == 0) && (KIND != kGemmMod || c == 0);
+                mma_f16(d_tmem, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), idesc, first ? 0u : 1u);
+              }
+              mma_commit(smem_u32(&empty[stage]));
+              ++consumed;
+              if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            if (ok) mma_commit(smem_u32(&accf[sl]));
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(kp.err, kErrTimeout);
+      }
+      // make sure no MMA is still writing TMEM before the final dealloc
+      mma_commit(smem_u32(drain));
+      mbar_wait_bounded(smem_u32(drain), 0, abort_flag, kWaitLimitNs);
+      *consumed_ctr = consumed;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t use[2] = {0, 0};
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
+      const Unit U = decode_unit(u, kp);
+      const int64_t i = static_cast<int64_t>(U.tm) * BM + row_in_tile;
+      const float mf = kp.mf[U.t];
+      const float inv_m = kp.inv_mf[U.t];
+      for (int c = 0; c < kp.nchunks && ok; ++c) {
+        const bool last = (c == kp.nchunks - 1);
+        for (int sl = 0; sl < U.ntile; ++sl) {
+          // every lane waits; the outcome is made warp-uniform so the
+          // .sync.aligned TMEM accesses below stay convergent
+          const bool got = mbar_wait_bounded(smem_u32(&accf[sl]), use[sl] & 1, abort_flag, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          ++use[sl];
+          tc_fence_after();
+          const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
+          const int64_t j0 = static_cast<int64_t>(U.tn0 + sl) * BN;
+          if (KIND == kGemmMod) {
+            if (!last) {
+              // in-place reduction: D <- D - m rint(D/m), exact in fp32
+#pragma unroll 1
+              for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(acc_addr + cb * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const float d = __uint_as_float(v[k]);
+                  const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
+                  v[k] = __float_as_uint(fmaf(-mf, q, d));
+                }
+                tmem_st32(acc_addr + cb * 32, v);
+              }
+              tmem_wait_st();
+            } else {
+              // final: R = D mod m in [0, m)
+              uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p * kp.r;
+#pragma unroll 1
+              for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(acc_addr + cb * 32, v);
+                tmem_wait_ld();
+                if (i < kp.p) {
+#pragma unroll
+                  for (int k = 0; k < 32; ++k) {
+                    const int64_t j = j0 + cb * 32 + k;
+                    const float d = __uint_as_float(v[k]);
+                    const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
+                    float rr = fmaf(-mf, q, d);
+                    rr = (rr < 0.0f) ? rr + mf : rr;
+                    if (j < kp.r) Rt[j * kp.p + i] = static_cast<uint8_t>(__float2uint_rn(rr));
+                  }
+                }
+              }
+            }
+          } else {
+            // drain the chunk into the int32 running sum at column offset +128
+            const uint32_t sum_addr = acc_addr + 128;
+#pragma unroll 1
+            for (int cb = 0; cb < BN / 32; ++cb) {
+              uint32_t v[32], sacc[32];
+              tmem_ld32(acc_addr + cb * 32, v);
+              if (c > 0) tmem_ld32(sum_addr + cb * 32, sacc);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const int add = __float2int_rn(__uint_as_float(v[k]));
+                sacc[k] = (c > 0) ? static_cast<uint32_t>(static_cast<int>(sacc[k]) + add)
+                                  : static_cast<uint32_t>(add);
+              }
+              if (!last) {
+                tmem_st32(sum_addr + cb * 32, sacc);
+              } else if (KIND == kGemmExactP) {
+                int32_t* Pt = kp.P + static_cast<int64_t>(U.t) * kp.p * kp.r;
+                if (i < kp.p) {
+#pragma unroll
+                  for (int k = 0; k < 32; ++k) {
+                    const int64_t j = j0 + cb * 32 + k;
+                    if (j < kp.r) Pt[j * kp.p + i] = static_cast<int32_t>(sacc[k]);
+                  }
+                }
+              } else {
+                // kGemmBound: row max of W 2^-v_j, column max of W 2^-u_i
+                const int ui = (i < kp.p) ? kp.u[i] : 0;
+                uint64_t rmax = 0;
+#pragma unroll 4
+                for (int k = 0; k < 32; ++k) {
+                  const int64_t j = j0 + cb * 32 + k;
+                  const bool valid = (i < kp.p) && (j < kp.r);
+                  const uint32_t w = valid ? sacc[k] : 0u;
+                  if (valid) {
+                    const uint64_t kr = dyadic_key(w, kp.v[j]);
+                    rmax = kr > rmax ? kr : rmax;
+                  }
+                  uint64_t kc = valid ? dyadic_key(w, ui) : 0ull;
+#pragma unroll
+                  for (int o = 16; o; o >>= 1) {
+                    const uint64_t x = __shfl_xor_sync(0xffffffffu, kc, o);
+                    kc = x > kc ? x : kc;
+                  }
+                  if (lane == 0 && kc && j < kp.r)
+                    atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + j),
+                              static_cast<unsigned long long>(kc));
+                }
+                if (rmax) atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i),
+                                    static_cast<unsigned long long>(rmax));
+              }
+            }
+            if (!last) tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&acce[sl]));
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      atomicOr(kp.err, kErrTimeout);
+    }
+  }
+
+  __syncthreads();
+  // On an abort, wait (bounded) for TMA loads still landing in shared memory.
+  if (threadIdx.x == 0 && *abort_flag) {
+    const int issued = *issued_ctr;
+    for (int k = *consumed_ctr; k < issued; ++k) {
+      const int st = k % C::STAGES;
+      const uint32_t ph = static_cast<uint32_t>((k / C::STAGES) & 1);
+      volatile int no_abort = 0;
+      if (!mbar_wait_bounded(smem_u32(&full[st]), ph, &no_abort, 100ull * 1000 * 1000)) break;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_plane_map(CUtensorMap* map, const uint16_t* base, int64_t qp, int64_t rows, int s,
+                    int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(qp), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(s)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(qp * 2), static_cast<cuuint64_t>(rows * qp * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int KIND>
+cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
+  using C = Cfg<BN>;
+  CUtensorMap ta, tb;
+  if (!make_plane_map(&ta, g.Aplanes, g.qp, g.p, g.s, BM)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&tb, g.Bplanes, g.qp, g.r, g.s, BN)) return cudaErrorInvalidValue;
+  KParams kp{};
+  kp.p = g.p;
+  kp.r = g.r;
+  kp.s = g.s;
+  kp.nkb = static_cast<int>(g.qp / BK);
+  kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
+  kp.tiles_m = static_cast<int>((g.p + BM - 1) / BM);
+  kp.tiles_n = static_cast<int>((g.r + BN - 1) / BN);
+  kp.pairs_n = (kp.tiles_n + 1) / 2;
+  kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
+  kp.R = g.R;
+  kp.P = g.P;
+  kp.rowkey = g.rowkey;
+  kp.colkey = g.colkey;
+  kp.u = g.u;
+  kp.v = g.v;
+  kp.err = g.err;
+  for (int t = 0; t < kSMax; ++t) {
+    kp.mf[t] = mc.mf[t];
+    kp.inv_mf[t] = mc.inv_mf[t];
+  }
+  auto kern = oz2_gemm_kernel<BN, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(kp.units, g.num_sms);
+  kern<<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM, st>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
+  switch (kind) {
+    case kGemmMod:
+      return launch_impl<256, kGemmMod>(g, mc, st);
+    case kGemmExactP:
+      return launch_impl<128, kGemmExactP>(g, mc, st);
+    case kGemmBound:
+      return launch_impl<128, kGemmBound>(g, mc, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace oz2

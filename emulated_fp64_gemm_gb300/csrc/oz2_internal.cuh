@@ -1,0 +1,196 @@
+// Internal declarations shared by the library's translation units.
+//
+// Kernels receive their constants by value (small parameter structs), so no
+// __constant__ symbol has to be shared across translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ozaki2.h"
+
+namespace oz2 {
+
+constexpr int kSMax = OZ2_S_MAX;
+// Multiword integers of the CRT stage: 5 x 32-bit limbs (160 bits).  With
+// s <= 20 the product M of the moduli is < 2^156 and sum_t w_t M/m_t < s M < 2^160.
+constexpr int kLimbs = 5;
+// Residue planes and bound planes store K (the inner dimension) padded to a
+// multiple of this, zero-filled, so every plane row is 16-byte aligned and
+// whole 64-wide K blocks can be fed to the tensor cores.
+constexpr int kKPad = 64;
+// Largest shift of the mantissa handled by the per-modulus power table.
+constexpr int kPow2Max = 2304;
+
+// Flags in the device error word.
+constexpr int kErrTimeout = 1;
+
+struct ModConsts {  // per-modulus constants, indexed by channel t
+  int s;
+  int m[kSMax];
+  int half[kSMax];                // floor(m/2)
+  uint32_t magic39[kSMax];        // ceil(2^39/m): floor(x/m) = umulhi(x, magic39) >> 7 for x < 2^31
+  uint32_t magic32[kSMax];        // ceil(2^32/m): floor(x/m) = umulhi(x, magic32) for x < 2^16
+  uint32_t w21[kSMax][3];         // 2^(21k) mod m, k = 0..2  (three 21-bit limbs)
+  uint32_t w20[kSMax][4];         // 2^(20k) mod m, k = 0..3  (four 20-bit limbs)
+  uint32_t KH[kSMax];             // K_m + floor(m/2), K_m = m ceil(2^30/m)
+  float mf[kSMax];                // m as float
+  float inv_mf[kSMax];            // fl(1/m)
+};
+
+struct CrtConsts {  // per-s CRT constants
+  int s;
+  int m[kSMax];
+  uint32_t inv[kSMax];            // (M/m_t)^-1 mod m_t
+  uint32_t magic32[kSMax];        // ceil(2^32/m)
+  uint32_t Mt[kSMax][kLimbs];     // M/m_t, little-endian 32-bit limbs
+  uint32_t M[kLimbs];             // M
+  uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
+  int top;                        // index of the top nonzero limb of M (>= 1)
+  float inv_Mtop;                 // 1 / (M_top64 as float), for the quotient estimate
+};
+
+struct BoundConsts {  // L = M/2 - 1 in the form the exponent kernels compare against
+  int Lbits;                      // bit length of L
+  uint64_t Lnorm;                 // L scaled so its top bit is bit 63 (exact when Lbits <= 64)
+};
+
+struct HostConsts {
+  ModConsts mod;
+  CrtConsts crt;
+  BoundConsts bound;
+};
+
+// Filled once per s (2..20) on the host.  Returns nullptr if s is out of range.
+const HostConsts* host_consts(int s);
+// The greedy moduli list (20 entries).
+const int* greedy_moduli20();
+
+// ---------------------------------------------------------------- launchers
+struct ScaleArgs {
+  int64_t p, q, r, lda, ldb;
+  const double* A;
+  const double* B;
+};
+
+// fast mode: alpha[p], beta[r]; uses amaxA/amaxB/sumA/sumB scratch.
+cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
+                                  uint64_t* amaxB, uint64_t* sumA, uint64_t* sumB, int32_t* alpha,
+                                  int32_t* beta, cudaStream_t st);
+
+// accu mode, first half: amax, quantised bound planes Abar [p][qp], Bbar [r][qp] (fp16),
+// and the quantisation exponents u[p], v[r].
+cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,
+                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar,
+                               cudaStream_t st);
+// accu mode, second half: exponents from the row / column max keys.
+cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,
+                                  const uint64_t* rowkey, const uint64_t* colkey, const int32_t* u,
+                                  const int32_t* v, int32_t* alpha, int32_t* beta, cudaStream_t st);
+
+// residue planes: A -> [s][p][qp], B -> [s][r][qp] (fp16 values in [-128, 127]).
+cudaError_t launch_residues(const ScaleArgs& a, int64_t qp, const ModConsts& mc,
+                            const int32_t* alpha, const int32_t* beta, const uint8_t* pow2mod,
+                            int max_bits_A, int max_bits_B, uint16_t* planesA,
+                            uint16_t* planesB, cudaStream_t st);
+
+// GEMM epilogue kinds
+enum GemmKind { kGemmMod = 0, kGemmExactP = 1, kGemmBound = 2 };
+
+struct GemmArgs {
+  int64_t p, r, qp;       // rows of A planes, rows of B planes, padded K
+  int s;                  // number of channels (planes)
+  const uint16_t* Aplanes;  // [s][p][qp]
+  const uint16_t* Bplanes;  // [s][r][qp]
+  uint8_t* R;             // kGemmMod: [s][r][p]
+  int32_t* P;             // kGemmExactP: [s][r][p]
+  uint64_t* rowkey;       // kGemmBound: [p]
+  uint64_t* colkey;       // kGemmBound: [r]
+  const int32_t* u;       // kGemmBound: [p]
+  const int32_t* v;       // kGemmBound: [r]
+  int* err;               // device error word
+  int num_sms;
+};
+
+cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st);
+
+// CRT + inverse scaling
+cudaError_t launch_crt(int64_t p, int64_t r, int s, const CrtConsts& cc, const uint8_t* R,
+                       const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
+                       uint64_t* X, cudaStream_t st);
+
+// debug copies
+cudaError_t launch_planes_to_int8(const uint16_t* planes, int64_t rows, int64_t q, int64_t qp,
+                                  int s, int8_t* out, cudaStream_t st);
+
+cudaError_t launch_wait_timeout_selftest(int* err, long long limit_ns, cudaStream_t st);
+
+}  // namespace oz2
+
+// ------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+namespace oz2 {
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of the given parity to complete.  Gives up (returns
+// false) after limit_ns of wall time or as soon as *abort is set, so no wait
+// in this library can spin forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}\n" ::"r"(addr)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}\n" ::"r"(addr),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+}  // namespace oz2
+#endif

@@ -1,0 +1,595 @@
+// Preprocessing kernels of the Ozaki-II pipeline: scaling statistics,
+// power-of-two exponents, accu-mode bound quantisation and the single-pass
+// residue planes.
+//
+// Method: "Profiling Ozaki II: The Cost Behind Fast INT8 GEMMs" §1 (green
+// stage), §2 (fast and accu bounds), §5.1 (row max-abs and sum of squares,
+// rounded up), §10.1 (convert each scaled element to an integer once, then
+// reduce it with fixed-divisor integer arithmetic per modulus).  Centered
+// residues: "Ozaki II supplement: INT8 range conditions and paper performance
+// results" §1.2.
+//
+// No floating-point arithmetic is used on the data: every double is taken
+// apart into its sign, exponent and 53-bit significand, and all statistics
+// and residues are exact integer computations.  This makes the exponents
+// independent of the order of the reductions (the statistics are u64 sums and
+// maxima) and removes the FP64 pipe from this stage.
+#include <cuda_fp16.h>
+
+#include "oz2_internal.cuh"
+
+namespace oz2 {
+namespace {
+
+constexpr int kF = 20;  // fractional bits of the fast-mode statistic
+
+struct Dec {  // |x| = mant * 2^E, mant < 2^53 (0 for x == 0), neg = sign bit
+  uint64_t mant;
+  int E;
+  uint32_t neg;
+};
+
+__device__ __forceinline__ Dec decode(double x) {
+  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x));
+  Dec d;
+  d.neg = static_cast<uint32_t>(b >> 63);
+  const int eb = static_cast<int>((b >> 52) & 0x7FF);
+  d.mant = b & ((1ull << 52) - 1);
+  if (eb == 0) {
+    d.E = -1074;
+  } else {
+    d.mant |= 1ull << 52;
+    d.E = eb - 1075;
+  }
+  return d;
+}
+
+// e = floor(log2 a) + 1 for a > 0 given as the bits of |a|; 0 for a == 0.
+__device__ __forceinline__ int exp_of_bits(uint64_t abits) {
+  if (abits == 0) return 0;
+  const int eb = static_cast<int>(abits >> 52);
+  if (eb != 0) return eb - 1022;
+  const uint64_t m = abits & ((1ull << 52) - 1);
+  return (63 - __clzll(static_cast<long long>(m))) - 1073;
+}
+
+// ceil(mant * 2^sh) for a result known to be < 2^63.
+__device__ __forceinline__ uint64_t ceil_shift(uint64_t mant, int sh) {
+  if (mant == 0) return 0;
+  if (sh >= 0) return mant << sh;
+  const int d = -sh;
+  if (d >= 64) return 1;
+  const uint64_t q = mant >> d;
+  return q + ((mant & ((1ull << d) - 1)) != 0 ? 1 : 0);
+}
+
+// max { h : S * 2^h <= L } for S > 0, with L given by (Lbits, Lnorm).
+__device__ __forceinline__ int max_shift_le_L(uint64_t S, const BoundConsts& bc) {
+  const int sb = 64 - __clzll(static_cast<long long>(S));
+  const uint64_t Snorm = S << (64 - sb);
+  const int k = bc.Lbits - sb;
+  return (Snorm <= bc.Lnorm) ? k : k - 1;
+}
+
+// ------------------------------------------------------------- statistics
+// Row max |a| of A (column-major p x q): threads along rows, columns split over blockIdx.y.
+__global__ void amax_rows_kernel(const double* __restrict__ A, int64_t p, int64_t q, int64_t lda,
+                                 int64_t cols_per_block, uint64_t* __restrict__ amax) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (i >= p) return;
+  const int64_t l0 = blockIdx.y * cols_per_block;
+  const int64_t l1 = min(q, l0 + cols_per_block);
+  uint64_t m = 0;
+  for (int64_t l = l0; l < l1; ++l) {
+    const uint64_t b = static_cast<uint64_t>(__double_as_longlong(A[l * lda + i])) & ~(1ull << 63);
+    m = b > m ? b : m;
+  }
+  if (m) atomicMax(reinterpret_cast<unsigned long long*>(amax + i), static_cast<unsigned long long>(m));
+}
+
+// Column max |b| of B (column-major q x r): one warp per (column, segment).
+__global__ void amax_cols_kernel(const double* __restrict__ B, int64_t q, int64_t r, int64_t ldb,
+                                 int64_t seg, uint64_t* __restrict__ amax) {
+  const int lane = threadIdx.x & 31;
+  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (j >= r) return;
+  const int64_t l0 = blockIdx.y * seg;
+  const int64_t l1 = min(q, l0 + seg);
+  uint64_t m = 0;
+  for (int64_t l = l0 + lane; l < l1; l += 32) {
+    const uint64_t b = static_cast<uint64_t>(__double_as_longlong(B[j * ldb + l])) & ~(1ull << 63);
+    m = b > m ? b : m;
+  }
+  for (int o = 16; o; o >>= 1) {
+    const uint64_t x = __shfl_xor_sync(0xffffffffu, m, o);
+    m = x > m ? x : m;
+  }
+  if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned long long*>(amax + j), static_cast<unsigned long long>(m));
+}
+
+// S = sum ceil(|a| 2^(F-e))^2 per row of A.
+__global__ void sumsq_rows_kernel(const double* __restrict__ A, int64_t p, int64_t q, int64_t lda,
+                                  int64_t cols_per_block, const uint64_t* __restrict__ amax,
+                                  uint64_t* __restrict__ sum) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (i >= p) return;
+  const int e = exp_of_bits(amax[i]);
+  const int64_t l0 = blockIdx.y * cols_per_block;
+  const int64_t l1 = min(q, l0 + cols_per_block);
+  uint64_t s = 0;
+  for (int64_t l = l0; l < l1; ++l) {
+    const Dec d = decode(A[l * lda + i]);
+    const uint64_t c = ceil_shift(d.mant, d.E + kF - e);
+    s += c * c;
+  }
+  if (s) atomicAdd(reinterpret_cast<unsigned long long*>(sum + i), static_cast<unsigned long long>(s));
+}
+
+__global__ void sumsq_cols_kernel(const double* __restrict__ B, int64_t q, int64_t r, int64_t ldb,
+                                  int64_t seg, const uint64_t* __restrict__ amax,
+                                  uint64_t* __restrict__ sum) {
+  const int lane = threadIdx.x & 31;
+  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (j >= r) return;
+  const int e = exp_of_bits(amax[j]);
+  const int64_t l0 = blockIdx.y * seg;
+  const int64_t l1 = min(q, l0 + seg);
+  uint64_t s = 0;
+  for (int64_t l = l0 + lane; l < l1; l += 32) {
+    const Dec d = decode(B[j * ldb + l]);
+    const uint64_t c = ceil_shift(d.mant, d.E + kF - e);
+    s += c * c;
+  }
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0 && s) atomicAdd(reinterpret_cast<unsigned long long*>(sum + j), static_cast<unsigned long long>(s));
+}
+
+// fast exponent: U = S 4^(e-F); exp = max { a : 4^a U <= L } = floor(h/2) - e + F,
+// h = max { h : S 2^h <= L }; 0 for a zero vector.
+__global__ void fast_exp_kernel(const uint64_t* __restrict__ amax, const uint64_t* __restrict__ sum,
+                                int64_t n, BoundConsts bc, int32_t* __restrict__ out) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (i >= n) return;
+  const uint64_t S = sum[i];
+  if (S == 0) {
+    out[i] = 0;
+    return;
+  }
+  const int e = exp_of_bits(amax[i]);
+  const int h = max_shift_le_L(S, bc);
+  out[i] = (h >> 1) - e + kF;  // arithmetic shift: floor(h/2)
+}
+
+// ------------------------------------------------------------- accu bound
+// u = max { u : ceil(amax 2^u) <= 127 } (0 for a zero vector).
+__device__ __forceinline__ int quant_exp(uint64_t abits) {
+  if (abits == 0) return 0;
+  const int e = exp_of_bits(abits);
+  uint64_t m = abits & ((1ull << 52) - 1);
+  if ((abits >> 52) != 0) {
+    m |= 1ull << 52;
+  } else {
+    m <<= (53 - (64 - __clzll(static_cast<long long>(m))));  // normalise to 53 bits
+  }
+  // amax * 2^(7-e) = m / 2^46 lies in [64, 128): it is <= 127 iff m <= 127 * 2^46.
+  return (m <= (127ull << 46)) ? 7 - e : 6 - e;
+}
+
+// Abar[i][l] = ceil(|a_il| 2^u_i) as fp16, K-major rows of length qp (zero padded).
+// Thread layout as in the residue kernel for A: 16 rows x 2 eight-element K groups per warp.
+__global__ void bound_quant_rows_kernel(const double* __restrict__ A, int64_t p, int64_t q,
+                                        int64_t lda, int64_t qp, const uint64_t* __restrict__ amax,
+                                        int32_t* __restrict__ u_out, uint16_t* __restrict__ Abar) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i = blockIdx.x * 32ll + (warp & 1) * 16 + (lane & 15);
+  const int64_t l0 = blockIdx.y * 64ll + (warp >> 1) * 16 + (lane >> 4) * 8;
+  if (i >= p || l0 >= qp) return;
+  const int u = quant_exp(amax[i]);
+  if (l0 == 0) u_out[i] = u;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    uint32_t c[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t l = l0 + k + h;
+      c[h] = 0;
+      if (l < q) {
+        const Dec d = decode(A[l * lda + i]);
+        c[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + u));
+      }
+    }
+    // fp16 of an integer c < 1024: bits 0x6400 + c encode 1024 + c; subtract 1024.
+    const uint32_t word = (c[1] << 16 | c[0]) + 0x64006400u;
+    __half2 hv = *reinterpret_cast<const __half2*>(&word);
+    hv = __hsub2(hv, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    w[k >> 1] = *reinterpret_cast<uint32_t*>(&hv);
+  }
+  *reinterpret_cast<uint4*>(Abar + i * qp + l0) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Bbar[j][l] = ceil(|b_lj| 2^v_j): one warp per column, 8 elements per lane.
+__global__ void bound_quant_cols_kernel(const double* __restrict__ B, int64_t q, int64_t r,
+                                        int64_t ldb, int64_t qp, const uint64_t* __restrict__ amax,
+                                        int32_t* __restrict__ v_out, uint16_t* __restrict__ Bbar) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t j = blockIdx.x * 8ll + warp;
+  const int64_t l0 = blockIdx.y * 256ll + lane * 8;
+  if (j >= r || l0 >= qp) return;
+  const int v = quant_exp(amax[j]);
+  if (l0 == 0) v_out[j] = v;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    uint32_t c[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t l = l0 + k + h;
+      c[h] = 0;
+      if (l < q) {
+        const Dec d = decode(B[j * ldb + l]);
+        c[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
+      }
+    }
+    const uint32_t word = (c[1] << 16 | c[0]) + 0x64006400u;
+    __half2 hv = *reinterpret_cast<const __half2*>(&word);
+    hv = __hsub2(hv, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    w[k >> 1] = *reinterpret_cast<uint32_t*>(&hv);
+  }
+  *reinterpret_cast<uint4*>(Bbar + j * qp + l0) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// accu exponents from the max keys of the bound GEMM.  A key encodes the
+// dyadic value w 2^-x (w < 2^31) as ((floor(log2) + 4096) << 32) | mantissa
+// normalised to 32 bits; 0 encodes zero.  The row value is
+// max_j Wbar_ij 2^-v_j, so U_i = value 2^-u_i; likewise for columns.
+__global__ void accu_exp_kernel(const uint64_t* __restrict__ key, const int32_t* __restrict__ qexp,
+                                int64_t n, BoundConsts bc, int32_t* __restrict__ out) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (i >= n) return;
+  const uint64_t k = key[i];
+  if (k == 0) {
+    out[i] = 0;
+    return;
+  }
+  const int E = static_cast<int>(k >> 32) - 4096;        // value = mant32 * 2^(E - 31)
+  const uint64_t mant = k & 0xffffffffull;
+  const int h = max_shift_le_L(mant, bc);                // mant 2^h <= L
+  // 4^a mant 2^(E - 31 - u) <= L  <=>  2a + E - 31 - u <= h
+  const int num = h - E + 31 + qexp[i];
+  out[i] = num >> 1;                                     // floor
+}
+
+// ------------------------------------------------------------- residues
+// Per element: the magnitude |trunc(2^e x)| = floor(mant 2^sh), sh = E + e, as
+// NL limbs of LB bits, each negated when x < 0.  Then, per modulus,
+//   T = l0 + sum_k w_k l_k + (K_m + floor(m/2)),  w_k = 2^(LB k) mod m,
+// K_m a multiple of m with K_m >= 2^30, so T is in [0, 2^31) and
+// T mod m = (trunc(2^e x) + floor(m/2)) mod m = rho_m(trunc(2^e x)) + floor(m/2).
+// The quotient comes from one multiply-high (magic39); the value goes to fp16
+// through the bit pattern 0x6400 + v (= 1024 + v) and a packed subtraction.
+template <int NL>
+struct Limbs {
+  int32_t l[NL];
+};
+
+template <int NL>
+__device__ __forceinline__ bool split_limbs(double x, int scale, Limbs<NL>& L, uint32_t& neg,
+                                            uint64_t& mant, int& sh) {
+  constexpr int LB = (NL == 3) ? 21 : 20;
+  const Dec d = decode(x);
+  neg = d.neg;
+  mant = d.mant;
+  sh = d.E + scale;
+  if (sh > LB * NL - 53) return false;  // does not fit NL limbs: general path
+#pragma unroll
+  for (int k = 0; k < NL; ++k) {
+    const int dd = LB * k - sh;
+    uint64_t v;
+    if (dd >= 0) v = (dd < 64) ? (d.mant >> dd) : 0ull;
+    else v = d.mant << (-dd);
+    const int32_t lv = static_cast<int32_t>(v & ((1ull << LB) - 1));
+    L.l[k] = d.neg ? -lv : lv;
+  }
+  return true;
+}
+
+// General path: rho_m(+-floor(mant 2^sh)) for sh > 0 via (mant mod m)(2^sh mod m).
+__device__ int residue_general(uint64_t mant, int sh, uint32_t neg, int t, const ModConsts& mc,
+                               const uint8_t* __restrict__ pow2mod) {
+  const uint32_t m = static_cast<uint32_t>(mc.m[t]);
+  uint32_t r;
+  if (m == 256) {
+    r = (sh >= 8) ? 0u : static_cast<uint32_t>((mant << sh) & 255u);
+  } else {
+    // mant mod m with 21-bit limbs (unsigned), then times 2^sh mod m
+    const uint32_t a0 = static_cast<uint32_t>(mant & 0x1FFFFF);
+    const uint32_t a1 = static_cast<uint32_t>((mant >> 21) & 0x1FFFFF);
+    const uint32_t a2 = static_cast<uint32_t>(mant >> 42);
+    const uint32_t T = a0 + mc.w21[t][1] * a1 + mc.w21[t][2] * a2;  // < 2^30
+    const uint32_t q = __umulhi(T, mc.magic39[t]) >> 7;
+    const uint32_t rm = T - q * m;
+    const int shc = sh < kPow2Max ? sh : kPow2Max - 1;
+    const uint32_t x = rm * pow2mod[t * kPow2Max + shc];  // < 2^16
+    r = x - __umulhi(x, mc.magic32[t]) * m;
+  }
+  if (neg) r = (r == 0) ? 0u : m - r;                   // nonnegative residue of the signed value
+  const int h = mc.half[t];
+  return static_cast<int>((r + static_cast<uint32_t>(h)) % m) - h;  // centered
+}
+
+
+// fp16 bits of two values v0, v1 in [0, 2048) shifted by -bias, packed (v0 low).
+__device__ __forceinline__ uint32_t pack_fp16_pair(uint32_t v0, uint32_t v1, __half2 bias2) {
+  const uint32_t word = (v1 << 16 | v0) + 0x64006400u;  // fp16(1024 + v)
+  __half2 hv = *reinterpret_cast<const __half2*>(&word);
+  hv = __hsub2(hv, bias2);                              // exact: integers below 2048
+  return *reinterpret_cast<uint32_t*>(&hv);
+}
+
+// Residues of 8 consecutive K elements of one plane row, for every modulus.
+// out points at row `row` of plane 0 (element offset l0 already applied);
+// consecutive planes are plane_stride elements apart.
+template <int NL>
+__device__ __forceinline__ void residues8(const double (&x)[8], int scale, const ModConsts& mc,
+                                          const uint8_t* __restrict__ pow2mod,
+                                          uint16_t* __restrict__ out, int64_t plane_stride) {
+  Limbs<NL> L[8];
+  uint32_t neg[8];
+  uint64_t mant[8];
+  int sh[8];
+  bool fast = true;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) fast &= split_limbs<NL>(x[e], scale, L[e], neg[e], mant[e], sh[e]);
+  const int s = mc.s;
+  if (fast) {
+    // channel 0: m = 256 (the greedy set always starts with 256), and
+    // 2^(LB k) = 0 mod 256 for k >= 1, so only the low limb matters.
+    {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t r0 = static_cast<uint32_t>(L[e].l[0] + 128) & 255u;
+        const uint32_t r1 = static_cast<uint32_t>(L[e + 1].l[0] + 128) & 255u;
+        w[e >> 1] = pack_fp16_pair(r0, r1, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+      }
+      *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    for (int t = 1; t < s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(mc.m[t]);
+      const uint32_t magic = mc.magic39[t];
+      const uint32_t KH = mc.KH[t];
+      uint32_t wk[NL];
+#pragma unroll
+      for (int k = 1; k < NL; ++k) wk[k] = (NL == 3) ? mc.w21[t][k] : mc.w20[t][k];
+      const __half hb = __ushort2half_rn(static_cast<unsigned short>(1024 + mc.half[t]));
+      const __half2 bias2 = __halves2half2(hb, hb);
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        uint32_t rr[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t T = static_cast<uint32_t>(L[e + h].l[0]) + KH;
+#pragma unroll
+          for (int k = 1; k < NL; ++k) T += wk[k] * static_cast<uint32_t>(L[e + h].l[k]);
+          const uint32_t q = __umulhi(T, magic) >> 7;
+          rr[h] = T - q * m;  // = rho_m(x') + floor(m/2)
+        }
+        w[e >> 1] = pack_fp16_pair(rr[0], rr[1], bias2);
+      }
+      *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    for (int t = 0; t < s; ++t) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        int v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ee = e + h;
+          if (sh[ee] <= ((NL == 3) ? 21 : 20) * NL - 53) {
+            // this element fits the limbs; reduce it the plain way
+            const uint32_t m = static_cast<uint32_t>(mc.m[t]);
+            int64_t acc = 0;
+#pragma unroll
+            for (int k = 0; k < NL; ++k)
+              acc += static_cast<int64_t>(L[ee].l[k]) *
+                     static_cast<int64_t>(k == 0 ? 1u : ((NL == 3) ? mc.w21[t][k] : mc.w20[t][k]));
+            int64_t rm = acc % static_cast<int64_t>(m);
+            if (rm < 0) rm += m;
+            const int hh = mc.half[t];
+            v[h] = static_cast<int>((rm + hh) % m) - hh;
+          } else {
+            v[h] = residue_general(mant[ee], sh[ee], neg[ee], t, mc, pow2mod);
+          }
+        }
+        const __half2 hv = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
+        w[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// A (column-major p x q) -> planes [s][p][qp]: each warp covers 16 rows x 16
+// K elements, so every load instruction reads two full 128-byte lines and
+// every row of every plane gets 32 contiguous bytes per warp store.
+template <int NL>
+__global__ void __launch_bounds__(256) residue_rows_kernel(const double* __restrict__ A, int64_t p,
+                                                           int64_t q, int64_t lda, int64_t qp,
+                                                           const int32_t* __restrict__ alpha,
+                                                           ModConsts mc,
+                                                           const uint8_t* __restrict__ pow2mod,
+                                                           uint16_t* __restrict__ planes) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i = blockIdx.x * 32ll + (warp & 1) * 16 + (lane & 15);
+  const int64_t l0 = blockIdx.y * 64ll + (warp >> 1) * 16 + (lane >> 4) * 8;
+  if (i >= p || l0 >= qp) return;
+  double x[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
+  residues8<NL>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, p * qp);
+}
+
+// B (column-major q x r) -> planes [s][r][qp]: one warp per column, 8
+// consecutive K elements per lane.
+template <int NL>
+__global__ void __launch_bounds__(256) residue_cols_kernel(const double* __restrict__ B, int64_t q,
+                                                           int64_t r, int64_t ldb, int64_t qp,
+                                                           const int32_t* __restrict__ beta,
+                                                           ModConsts mc,
+                                                           const uint8_t* __restrict__ pow2mod,
+                                                           uint16_t* __restrict__ planes) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t j = blockIdx.x * 8ll + warp;
+  const int64_t l0 = blockIdx.y * 256ll + lane * 8;
+  if (j >= r || l0 >= qp) return;
+  const double* col = B + j * ldb + l0;
+  double x[8];
+  if (l0 + 8 <= q && (reinterpret_cast<uintptr_t>(col) & 15) == 0) {
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      const double2 v = __ldg(reinterpret_cast<const double2*>(col + k));
+      x[k] = v.x;
+      x[k + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(col + k) : 0.0;
+  }
+  residues8<NL>(x, beta[j], mc, pow2mod, planes + j * qp + l0, r * qp);
+}
+
+__global__ void planes_to_int8_kernel(const uint16_t* __restrict__ planes, int64_t rows, int64_t q,
+                                      int64_t qp, int s, int8_t* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(s) * rows * q;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t l = idx % q;
+    const int64_t rt = idx / q;  // t * rows + row
+    const uint16_t b = planes[rt * qp + l];
+    out[idx] = static_cast<int8_t>(__half2int_rn(__ushort_as_half(b)));
+  }
+}
+
+// One block waits on an mbarrier that nothing completes; the bounded wait
+// must give up, flag the error word and let the kernel exit.
+__global__ void wait_timeout_selftest_kernel(int* err, long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, static_cast<uint64_t>(limit_ns)))
+      atomicOr(err, kErrTimeout);
+  }
+  __syncthreads();
+}
+
+int cols_split(int64_t q, int64_t blocks_other, int num_sms) {
+  // enough blocks for ~4 waves, but at least 64 elements per thread
+  int64_t want = (4ll * num_sms + blocks_other - 1) / blocks_other;
+  int64_t maxs = (q + 63) / 64;
+  if (want > maxs) want = maxs;
+  if (want < 1) want = 1;
+  if (want > 65535) want = 65535;
+  return static_cast<int>(want);
+}
+
+int device_sms() {
+  int dev = 0, n = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- launchers
+cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
+                                  uint64_t* amaxB, uint64_t* sumA, uint64_t* sumB, int32_t* alpha,
+                                  int32_t* beta, cudaStream_t st) {
+  const int sms = device_sms();
+  cudaMemsetAsync(amaxA, 0, a.p * sizeof(uint64_t), st);
+  cudaMemsetAsync(amaxB, 0, a.r * sizeof(uint64_t), st);
+  cudaMemsetAsync(sumA, 0, a.p * sizeof(uint64_t), st);
+  cudaMemsetAsync(sumB, 0, a.r * sizeof(uint64_t), st);
+  const int64_t rb = (a.p + 255) / 256;
+  const int splitA = cols_split(a.q, rb, sms);
+  const int64_t cpbA = (a.q + splitA - 1) / splitA;
+  const int64_t cb = (a.r + 7) / 8;
+  const int splitB = cols_split(a.q, cb, sms);
+  const int64_t segB = (a.q + splitB - 1) / splitB;
+  amax_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA);
+  amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
+  sumsq_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA, sumA);
+  sumsq_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB, sumB);
+  fast_exp_kernel<<<static_cast<unsigned>((a.p + 255) / 256), 256, 0, st>>>(amaxA, sumA, a.p, bc, alpha);
+  fast_exp_kernel<<<static_cast<unsigned>((a.r + 255) / 256), 256, 0, st>>>(amaxB, sumB, a.r, bc, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,
+                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar,
+                               cudaStream_t st) {
+  const int sms = device_sms();
+  cudaMemsetAsync(amaxA, 0, a.p * sizeof(uint64_t), st);
+  cudaMemsetAsync(amaxB, 0, a.r * sizeof(uint64_t), st);
+  const int64_t rb = (a.p + 255) / 256;
+  const int splitA = cols_split(a.q, rb, sms);
+  const int64_t cpbA = (a.q + splitA - 1) / splitA;
+  const int64_t cb = (a.r + 7) / 8;
+  const int splitB = cols_split(a.q, cb, sms);
+  const int64_t segB = (a.q + splitB - 1) / splitB;
+  amax_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA);
+  amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
+  bound_quant_rows_kernel<<<dim3(static_cast<unsigned>((a.p + 31) / 32), static_cast<unsigned>(qp / 64)), 256, 0, st>>>(
+      a.A, a.p, a.q, a.lda, qp, amaxA, u, Abar);
+  bound_quant_cols_kernel<<<dim3(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256)), 256, 0, st>>>(
+      a.B, a.q, a.r, a.ldb, qp, amaxB, v, Bbar);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,
+                                  const uint64_t* rowkey, const uint64_t* colkey, const int32_t* u,
+                                  const int32_t* v, int32_t* alpha, int32_t* beta, cudaStream_t st) {
+  accu_exp_kernel<<<static_cast<unsigned>((p + 255) / 256), 256, 0, st>>>(rowkey, u, p, bc, alpha);
+  accu_exp_kernel<<<static_cast<unsigned>((r + 255) / 256), 256, 0, st>>>(colkey, v, r, bc, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residues(const ScaleArgs& a, int64_t qp, const ModConsts& mc,
+                            const int32_t* alpha, const int32_t* beta, const uint8_t* pow2mod,
+                            int max_bits_A, int max_bits_B, uint16_t* planesA, uint16_t* planesB,
+                            cudaStream_t st) {
+  const dim3 gA(static_cast<unsigned>((a.p + 31) / 32), static_cast<unsigned>(qp / 64));
+  const dim3 gB(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256));
+  if (max_bits_A <= 63)
+    residue_rows_kernel<3><<<gA, 256, 0, st>>>(a.A, a.p, a.q, a.lda, qp, alpha, mc, pow2mod, planesA);
+  else
+    residue_rows_kernel<4><<<gA, 256, 0, st>>>(a.A, a.p, a.q, a.lda, qp, alpha, mc, pow2mod, planesA);
+  if (max_bits_B <= 63)
+    residue_cols_kernel<3><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
+  else
+    residue_cols_kernel<4><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_planes_to_int8(const uint16_t* planes, int64_t rows, int64_t q, int64_t qp,
+                                  int s, int8_t* out, cudaStream_t st) {
+  planes_to_int8_kernel<<<1024, 256, 0, st>>>(planes, rows, q, qp, s, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(int* err, long long limit_ns, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace oz2

@@ -1,0 +1,165 @@
+/*
+ * ozaki2.h — C ABI of the GB300 (sm_103a) Ozaki Scheme II FP64 GEMM.
+ *
+ * The library computes C = A B for FP64 matrices through s small integer
+ * channels, following the pipeline of "Profiling Ozaki II: The Cost Behind
+ * Fast INT8 GEMMs" (§1, pipeline table) and "Ozaki II supplement: INT8 range
+ * conditions and paper performance results" (§1.1):
+ *
+ *   1. choose power-of-two row scales D = diag(2^alpha_i) and column scales
+ *      E = diag(2^beta_j) from a bound on |A||B| (fast: Cauchy–Schwarz norm
+ *      bound; accu: one extra integer bound GEMM — "Profiling Ozaki II" §2),
+ *   2. A' = trunc(D A), B' = trunc(B E), then the centered residues
+ *      A_t = rho_{m_t}(A'), B_t = rho_{m_t}(B') for s pairwise-coprime
+ *      moduli m_t <= 256 (supplement §1.2),
+ *   3. P_t = A_t B_t exactly, R_t = P_t mod m_t in [0, m_t),
+ *   4. X = CRT_M(R_1..R_s) in [-M/2, M/2), C = D^-1 X E^-1.
+ *
+ * Moduli: the s largest integers <= 256 taken greedily, each coprime to all
+ * larger ones kept (256, 255, 253, 251, 247, 241, 239, 233, ...).
+ *
+ * Layouts: every matrix is column-major.  A is p x q with leading dimension
+ * lda >= p, B is q x r (ldb >= q), C is p x r (ldc >= p).  C is overwritten
+ * (there are no BLAS alpha/beta scalars).  A, B and C are caller-owned device
+ * memory (ozaki2_dgemm_host excepted) and C must not overlap A or B.
+ *
+ * Asynchrony: ozaki2_dgemm enqueues all its kernels on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream) and returns without
+ * synchronising.  Argument errors are returned before anything is enqueued.
+ *
+ * Workspace: intermediate planes, residues and exponents live in a
+ * library-owned device workspace, one per (device, stream) pair, grown on
+ * demand and kept for later calls.  Growing it synchronises the device.
+ * Calls on the same stream are ordered; calls that share a stream's
+ * workspace must not run concurrently from several host threads.
+ *
+ * Preconditions: finite inputs (an Inf/NaN entry gives an unspecified
+ * result in its row of C / column of C), q < 131072 (the INT32 condition of
+ * supplement §1.3, kept as the library's contract), 2 <= s <= 20.
+ */
+#ifndef OZAKI2_H
+#define OZAKI2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OZ2_FAST = 0, /* row/column norm bound (Cauchy–Schwarz) */
+  OZ2_ACCU = 1  /* one extra bound GEMM on upward-quantised |A|, |B| */
+} oz2_mode;
+
+typedef enum {
+  OZ2_OK = 0,
+  OZ2_ERR_INVALID_ARG = 1,       /* bad size, leading dimension, pointer, s or mode */
+  OZ2_ERR_Q_TOO_LARGE = 2,       /* q >= 131072 */
+  OZ2_ERR_NO_MEMORY = 3,         /* workspace allocation failed */
+  OZ2_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+  OZ2_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait gave up */
+  OZ2_ERR_UNSUPPORTED_DEVICE = 6 /* the current device is not sm_103 */
+} oz2_status;
+
+/* Smallest and largest number of moduli accepted. */
+#define OZ2_S_MIN 2
+#define OZ2_S_MAX 20
+/* Exclusive upper bound on the inner dimension q. */
+#define OZ2_Q_LIMIT 131072
+
+/*
+ * C = A B by Ozaki Scheme II with s moduli and the given bound mode.
+ * A, B, C: device pointers.  stream: cudaStream_t (may be NULL).
+ * Returns OZ2_OK once every kernel is enqueued; see the file comment for
+ * the errors returned synchronously.
+ */
+oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r,
+                        const double* A, int64_t lda,
+                        const double* B, int64_t ldb,
+                        double* C, int64_t ldc,
+                        int s, int mode, void* stream);
+
+/*
+ * The same pipeline, run by the same kernels, with each stage's output
+ * copied out for checking.  Every output pointer may be NULL (skipped).
+ * All are device pointers, owned by the caller:
+ *   alpha [p] int32, beta [r] int32   — the exponents of D and E;
+ *   Ares  [s][p][q] int8              — rho_{m_t}(A'), row-major per plane;
+ *   Bres  [s][r][q] int8              — rho_{m_t}(B'), column j contiguous;
+ *   P     [s][r][p] int32             — A_t B_t, column-major per plane
+ *                                       (computed by an extra GEMM launch
+ *                                       that keeps exact sums);
+ *   R     [s][r][p] uint8             — P_t mod m_t, column-major per plane;
+ *   X     [r][p][3] uint64            — CRT integer, 192-bit two's
+ *                                       complement, little-endian limbs,
+ *                                       column-major over (i, j).
+ * The call synchronises `stream` before returning.
+ */
+oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r,
+                              const double* A, int64_t lda,
+                              const double* B, int64_t ldb,
+                              double* C, int64_t ldc,
+                              int s, int mode, void* stream,
+                              int32_t* alpha, int32_t* beta,
+                              int8_t* Ares, int8_t* Bres,
+                              int32_t* P, uint8_t* R, uint64_t* X);
+
+/*
+ * ozaki2_dgemm with CUDA events recorded between its stages; synchronises
+ * `stream` and writes the milliseconds of each stage to stage_ms[0..5]:
+ *   0 scale statistics and exponents (fast) or bound quantisation (accu)
+ *   1 bound GEMM and exponents (accu; 0 in fast mode)
+ *   2 residue planes of A and B
+ *   3 the s modular GEMMs with the fused mod-m_t epilogue
+ *   4 CRT and inverse scaling
+ *   5 the whole call
+ */
+oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r,
+                               const double* A, int64_t lda,
+                               const double* B, int64_t ldb,
+                               double* C, int64_t ldc,
+                               int s, int mode, void* stream, float* stage_ms);
+
+/*
+ * Host-memory variant: A, B and C are HOST pointers (pinned memory gives the
+ * fastest copies).  The library copies A and B into a device staging area of
+ * its workspace, runs ozaki2_dgemm on `stream`, copies C back, and
+ * synchronises `stream` before returning.
+ */
+oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
+                             const double* A, int64_t lda,
+                             const double* B, int64_t ldb,
+                             double* C, int64_t ldc,
+                             int s, int mode, void* stream);
+
+/* Writes the s moduli to out[0..s-1]; returns s, or -1 if s is out of range. */
+int ozaki2_moduli(int s, int32_t* out);
+
+/*
+ * Sticky device-side error word: OZ2_ERR_DEVICE_TIMEOUT if a bounded wait in
+ * any kernel that has completed gave up since the last call, else OZ2_OK.
+ * Reading it clears it.  Synchronise the stream first to include its work.
+ */
+oz2_status ozaki2_last_error(void);
+
+/* Frees every workspace of every device (synchronises each device first). */
+void ozaki2_workspace_release(void);
+
+/* Static text for a status code. */
+const char* ozaki2_status_string(oz2_status status);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one block that waits on
+ * a barrier nothing completes, with a wait limit of about `limit_us`
+ * microseconds (1..1000000).  It returns OZ2_ERR_DEVICE_TIMEOUT when the
+ * wait gave up as designed and the kernel exited cleanly, OZ2_OK if it did
+ * not (a bug), or OZ2_ERR_CUDA.  Synchronises the device.
+ */
+oz2_status ozaki2_selftest_wait_timeout(int limit_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OZAKI2_H */

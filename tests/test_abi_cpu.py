@@ -1,0 +1,68 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every declared entry point; host logic (moduli, argument checks)
+behaves as documented; without a GPU the product path fails loudly."""
+import ctypes
+
+import pytest
+
+import emulated_fp64_gemm_gb300 as oz2
+from emulated_fp64_gemm_gb300 import _build
+from oracle import ozaki2_oracle as oracle
+from tests._util import header_functions
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return oz2.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_moduli_match_oracle(lib):
+    for s in range(oz2.S_MIN, oz2.S_MAX + 1):
+        assert oz2.moduli(s) == oracle.greedy_moduli(s)
+    with pytest.raises(ValueError):
+        oz2.moduli(1)
+    with pytest.raises(ValueError):
+        oz2.moduli(21)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.ozaki2_status_string(code)
+
+
+def _call(lib, p=4, q=4, r=4, A=1, lda=4, B=1, ldb=4, C=1, ldc=4, s=8, mode=0):
+    vp = ctypes.c_void_p
+    return lib.ozaki2_dgemm(p, q, r, vp(A), lda, vp(B), ldb, vp(C), ldc, s, mode, vp(0))
+
+
+def test_argument_errors_are_returned_before_any_device_work(lib):
+    assert _call(lib, p=0) == 1
+    assert _call(lib, q=-1) == 1
+    assert _call(lib, r=0) == 1
+    assert _call(lib, lda=3) == 1
+    assert _call(lib, ldb=3) == 1
+    assert _call(lib, ldc=3) == 1
+    assert _call(lib, A=0) == 1
+    assert _call(lib, B=0) == 1
+    assert _call(lib, C=0) == 1
+    assert _call(lib, s=1) == 1
+    assert _call(lib, s=21) == 1
+    assert _call(lib, mode=2) == 1
+    assert _call(lib, q=131072, ldb=131072) == 2  # the INT32 condition q < 2^17
+    assert _call(lib, q=131071, ldb=131071) != 2
+
+
+def test_no_gpu_means_a_loud_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(lib) == 4  # OZ2_ERR_CUDA: there is no CPU fallback

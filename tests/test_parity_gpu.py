@@ -1,0 +1,209 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Integer stages (exponents, residue planes, products, output residues, CRT
+integer) must match bit for bit; C within 2 ulp (|ord(a) - ord(b)| <= 2 on
+the sign-magnitude order of the bit patterns).  Small and medium cases are
+compared element by element; the full-size workloads are compared on their
+exponents and on sampled outputs computed one by one by the oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import ozaki2_oracle as oracle
+from tests._util import decode_x, ulp_distance
+from workloads import WORKLOADS, make_matrices, make_workload
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ULP_TOL = 2
+
+
+@pytest.fixture(scope="module")
+def oz2():
+    import __graft_entry__ as g
+
+    g.build()
+    import emulated_fp64_gemm_gb300 as m
+
+    assert torch.cuda.is_available()
+    return m
+
+
+def _dev(x):
+    return torch.from_numpy(np.asfortranarray(x)).cuda()
+
+
+def _full_check(oz2, A, B, s, mode, check_p=True):
+    got = oz2.dgemm_debug(_dev(A), _dev(B), s, mode, want_p=check_p)
+    torch.cuda.synchronize()
+    ref = oracle.oracle_dgemm(A, B, s, mode)
+    np.testing.assert_array_equal(got["alpha"].cpu().numpy(), ref["alpha"], err_msg="alpha")
+    np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref["beta"], err_msg="beta")
+    np.testing.assert_array_equal(got["Ares"].cpu().numpy(), ref["Ares"], err_msg="A residues")
+    np.testing.assert_array_equal(got["Bres"].cpu().numpy(), np.transpose(ref["Bres"], (0, 2, 1)),
+                                  err_msg="B residues")
+    if check_p:
+        np.testing.assert_array_equal(got["P"].cpu().numpy(), np.transpose(ref["P"], (0, 2, 1)),
+                                      err_msg="products")
+    np.testing.assert_array_equal(got["R"].cpu().numpy(), np.transpose(ref["R"], (0, 2, 1)),
+                                  err_msg="output residues")
+    X = got["X"].cpu().numpy()
+    p, r = ref["X"].shape
+    for i in range(p):
+        for j in range(r):
+            assert decode_x(X[j, i]) == ref["X"][i, j], ("X", i, j)
+    C = got["C"].cpu().numpy()
+    assert ulp_distance(C, ref["C"]) <= ULP_TOL
+    # the production entry point gives the same C as the checking one
+    C2 = oz2.dgemm(_dev(A), _dev(B), s, mode).cpu().numpy()
+    np.testing.assert_array_equal(C2, C)
+    assert oz2.last_error() == 0
+    return got, ref
+
+
+def test_bounded_wait_gives_up_and_reports(oz2):
+    # a barrier that nothing completes: the wait must end with a timeout status
+    assert oz2.selftest_wait_timeout(2000) == 5
+    assert oz2.selftest_wait_timeout(50) == 5
+
+
+def test_small_workload_every_stage(oz2):
+    w = WORKLOADS["n128_s8_fast"]
+    A, B = make_workload(w)
+    _full_check(oz2, A, B, w.s, w.mode)
+
+
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+@pytest.mark.parametrize("p,q,r,s", [
+    (1, 1, 1, 2), (7, 13, 5, 8), (129, 1000, 257, 14), (1000, 129, 7, 18),
+    (300, 70, 513, 20), (64, 961, 40, 14), (130, 1921, 260, 16), (257, 64, 1, 3),
+])
+def test_ragged_shapes(oz2, p, q, r, s, mode):
+    A, B = make_matrices(p, q, r, 1.0, p * 1000 + q + r + s)
+    _full_check(oz2, A, B, s, mode)
+
+
+def test_leading_dimensions_larger_than_rows(oz2):
+    A, B = make_matrices(150, 90, 70, 0.5, 3)
+    bigA = torch.zeros((200, 90), dtype=torch.float64).t().contiguous().t()  # strides (1, 200)
+    bigA[:150] = torch.from_numpy(A)
+    bigB = torch.zeros((100, 70), dtype=torch.float64).t().contiguous().t()
+    bigB[:90] = torch.from_numpy(B)
+    dA = bigA.cuda()[:150]
+    dB = bigB.cuda()[:90]
+    assert dA.stride() == (1, 200) and dB.stride() == (1, 100)
+    C = oz2.dgemm(dA, dB, 14, "fast").cpu().numpy()
+    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    assert ulp_distance(C, ref["C"]) <= ULP_TOL
+    Cbig = torch.full((160, 70), 7.0, dtype=torch.float64).t().contiguous().t().cuda()  # ldc = 160
+    oz2.dgemm(dA, dB, 14, "fast", out=Cbig[:150])
+    Cb = Cbig.cpu().numpy()
+    assert ulp_distance(Cb[:150], ref["C"]) <= ULP_TOL
+    assert np.all(Cb[150:] == 7.0)  # rows past p untouched
+
+
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+def test_special_values(oz2, mode):
+    A, B = make_matrices(96, 200, 80, 2.0, 5)
+    A[3, :] = 0.0                      # zero row
+    B[:, 4] = 0.0                      # zero column
+    A[5, :] *= 1e-310                  # subnormal row
+    A[6, 7] = 1e300                    # one huge entry
+    A[7, :] = -A[7, :] * 2.0**600
+    B[11, :] = 5e-324                  # smallest subnormals
+    B[:, 9] *= 2.0**-1000
+    A[8, ::2] = -0.0
+    _full_check(oz2, A, B, 14, mode)
+
+
+def test_wide_range_accu_general_residue_path(oz2):
+    """A huge entry meeting only zeros of B: trunc(2^alpha a) needs the general residue path."""
+    A, B = make_matrices(40, 64, 30, 1.0, 8)
+    A[2, :] = 0.0
+    A[2, 0] = 1e300
+    B[0, :] = 0.0
+    got, ref = _full_check(oz2, A, B, 14, "accu")
+    assert ref["alpha"][2] == 0
+
+
+def test_small_integer_inputs_exact(oz2):
+    rng = np.random.default_rng(3)
+    A = rng.integers(-8, 9, size=(200, 300)).astype(np.float64)
+    B = rng.integers(-8, 9, size=(300, 100)).astype(np.float64)
+    C = oz2.dgemm(_dev(A), _dev(B), 8, "fast").cpu().numpy()
+    np.testing.assert_array_equal(C, (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64))
+
+
+def test_row_major_operands(oz2):
+    A, B = make_matrices(70, 50, 60, 0.5, 4)
+    dA = torch.from_numpy(np.ascontiguousarray(A)).cuda()  # row-major
+    dB = torch.from_numpy(np.ascontiguousarray(B)).cuda()
+    C = oz2.dgemm(dA, dB, 14, "fast").cpu().numpy()
+    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    assert ulp_distance(C, ref["C"]) <= ULP_TOL
+
+
+def test_host_entry_point(oz2):
+    A, B = make_matrices(300, 200, 100, 0.5, 6)
+    hA = torch.from_numpy(np.asfortranarray(A)).pin_memory()
+    hB = torch.from_numpy(np.asfortranarray(B)).pin_memory()
+    C = oz2.dgemm_host(hA, hB, 14, "fast").numpy()
+    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    assert ulp_distance(C, ref["C"]) <= ULP_TOL
+
+
+def test_stage_timing_entry_point(oz2):
+    A, B = make_matrices(256, 256, 256, 0.5, 2)
+    for mode in ("fast", "accu"):
+        C, ms = oz2.dgemm_stages(_dev(A), _dev(B), 14, mode)
+        ref = oracle.oracle_dgemm(A, B, 14, mode)
+        assert ulp_distance(C.cpu().numpy(), ref["C"]) <= ULP_TOL
+        assert ms["total"] > 0 and all(v >= 0 for v in ms.values())
+
+
+def test_n1024_workload_every_stage(oz2):
+    w = WORKLOADS["n1024_s14_fast"]
+    A, B = make_workload(w)
+    _full_check(oz2, A, B, w.s, w.mode)
+
+
+def _sampled_check(oz2, name, nsamp=384):
+    w = WORKLOADS[name]
+    A, B = make_workload(w)
+    dA, dB = _dev(A), _dev(B)
+    # the launch configuration the benchmark times: the production entry point
+    C = oz2.dgemm(dA, dB, w.s, w.mode)
+    got = oz2.dgemm_debug(dA, dB, w.s, w.mode, want_p=False)
+    torch.cuda.synchronize()
+    alpha, beta, _ = oracle.exponents(A, B, w.s, w.mode)
+    np.testing.assert_array_equal(got["alpha"].cpu().numpy(), alpha, err_msg="alpha")
+    np.testing.assert_array_equal(got["beta"].cpu().numpy(), beta, err_msg="beta")
+    rng = np.random.default_rng(99)
+    ii = rng.integers(0, w.p, nsamp)
+    jj = rng.integers(0, w.r, nsamp)
+    ii[:4] = [0, w.p - 1, 0, w.p - 1]
+    jj[:4] = [0, 0, w.r - 1, w.r - 1]
+    ref = oracle.oracle_entries(A, B, w.s, w.mode, ii, jj, alpha=alpha, beta=beta)
+    ti = torch.from_numpy(ii).cuda()
+    tj = torch.from_numpy(jj).cuda()
+    Cs = C[ti, tj].cpu().numpy()
+    assert ulp_distance(Cs, ref["C"]) <= ULP_TOL
+    Rs = got["R"][:, tj, ti].cpu().numpy()
+    np.testing.assert_array_equal(Rs, ref["R"])
+    Xs = got["X"][tj, ti].cpu().numpy()
+    for k in range(nsamp):
+        assert decode_x(Xs[k]) == ref["X"][k], k
+    # residue planes on the sampled rows / columns
+    rows = torch.from_numpy(ref["rows"]).cuda()
+    cols = torch.from_numpy(ref["cols"]).cuda()
+    np.testing.assert_array_equal(got["Ares"][:, rows, :].cpu().numpy(), ref["Arows"])
+    np.testing.assert_array_equal(got["Bres"][:, cols, :].cpu().numpy(), np.transpose(ref["Bcols"], (0, 2, 1)))
+    assert oz2.last_error() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["n4096_s14_accu", "n8192_s14_fast", "n8192_s14_accu",
+                                  "n8192_s18_fast", "n8192_s18_accu", "p16384_q8192_r16384_s18_accu"])
+def test_full_size_workloads_sampled(oz2, name):
+    _sampled_check(oz2, name)
