@@ -18,7 +18,7 @@ import os
 __all__ = [
     "FAST", "ACCU", "Ozaki2Error", "load_library", "library_path", "moduli", "dgemm",
     "dgemm_debug", "dgemm_stages", "dgemm_host", "last_error", "workspace_release",
-    "selftest_wait_timeout", "STAGE_NAMES",
+    "selftest_wait_timeout", "STAGE_NAMES", "profile_begin", "profile_end", "launch_count",
 ]
 
 FAST = 0
@@ -73,6 +73,12 @@ def load_library():
     lib.ozaki2_workspace_release.restype = None
     lib.ozaki2_status_string.argtypes = [i32]
     lib.ozaki2_status_string.restype = ctypes.c_char_p
+    lib.ozaki2_profile_begin.argtypes = [i32]
+    lib.ozaki2_profile_begin.restype = i32
+    lib.ozaki2_profile_end.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+    lib.ozaki2_profile_end.restype = i32
+    lib.ozaki2_launch_count.argtypes = []
+    lib.ozaki2_launch_count.restype = ctypes.c_uint64
     lib.ozaki2_selftest_wait_timeout.argtypes = [i32]
     lib.ozaki2_selftest_wait_timeout.restype = i32
     _lib = lib
@@ -233,6 +239,24 @@ def dgemm_host(A, B, s: int = 14, mode="fast", out=None, stream=None):
     _check(lib.ozaki2_dgemm_host(p, q, r, a[0], a[1], b[0], b[1], c[0], c[1], int(s), _mode(mode),
                                  _stream_handle(stream)), "ozaki2_dgemm_host")
     return out
+
+
+def profile_begin(max_calls: int) -> None:
+    """Record stage events in the next max_calls dgemm calls (no synchronisation)."""
+    _check(load_library().ozaki2_profile_begin(int(max_calls)), "ozaki2_profile_begin")
+
+
+def profile_end():
+    """(calls, {stage: summed ms}) of the calls recorded since profile_begin."""
+    ms = (ctypes.c_float * 6)()
+    n = ctypes.c_int(0)
+    _check(load_library().ozaki2_profile_end(ms, ctypes.byref(n)), "ozaki2_profile_end")
+    return n.value, dict(zip(STAGE_NAMES, [float(x) for x in ms]))
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load_library().ozaki2_launch_count())
 
 
 def last_error() -> int:

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -187,6 +188,15 @@ struct Workspace {
 };
 
 std::mutex g_mutex;
+std::atomic<uint64_t> g_launches{0};
+
+struct Profile {
+  bool on = false;
+  int max_calls = 0;
+  std::vector<cudaEvent_t> ev;  // 6 per recorded call
+  int used = 0;
+};
+Profile g_prof;
 std::map<int, DeviceState> g_dev;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
@@ -413,6 +423,8 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
 
 }  // namespace
 
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
 const HostConsts* host_consts(int s) {
   if (s < OZ2_S_MIN || s > kSMax) return nullptr;
   return &tables().hc[s];
@@ -433,9 +445,54 @@ oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r, const double* A, int64_
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
   if (e != OZ2_OK) return e;
   std::lock_guard<std::mutex> lk(g_mutex);
+  cudaEvent_t* ev = nullptr;
+  if (g_prof.on && g_prof.used < g_prof.max_calls) ev = &g_prof.ev[static_cast<size_t>(g_prof.used++) * 6];
   return run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, static_cast<cudaStream_t>(stream),
-                      nullptr, nullptr, nullptr, nullptr);
+                      nullptr, ev, nullptr, nullptr);
 }
+
+oz2_status ozaki2_profile_begin(int max_calls) {
+  if (max_calls < 1 || max_calls > 100000) return OZ2_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.assign(static_cast<size_t>(max_calls) * 6, nullptr);
+  for (auto& e : g_prof.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return OZ2_ERR_CUDA;
+  g_prof.max_calls = max_calls;
+  g_prof.used = 0;
+  g_prof.on = true;
+  return OZ2_OK;
+}
+
+oz2_status ozaki2_profile_end(float* stage_ms_sum, int* ncalls) {
+  if (!stage_ms_sum || !ncalls) return OZ2_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  for (int k = 0; k < 6; ++k) stage_ms_sum[k] = 0.0f;
+  oz2_status res = OZ2_OK;
+  for (int c = 0; c < g_prof.used; ++c) {
+    cudaEvent_t* e = &g_prof.ev[static_cast<size_t>(c) * 6];
+    if (cudaEventSynchronize(e[5]) != cudaSuccess) {
+      res = OZ2_ERR_CUDA;
+      break;
+    }
+    for (int k = 0; k < 5; ++k) {
+      float ms = 0.0f;
+      cudaEventElapsedTime(&ms, e[k], e[k + 1]);
+      stage_ms_sum[k] += ms;
+    }
+    float tot = 0.0f;
+    cudaEventElapsedTime(&tot, e[0], e[5]);
+    stage_ms_sum[5] += tot;
+  }
+  *ncalls = g_prof.used;
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.on = false;
+  g_prof.used = 0;
+  return res;
+}
+
+uint64_t ozaki2_launch_count(void) { return g_launches.load(); }
 
 oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
                               const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,

@@ -198,6 +198,7 @@ cudaError_t launch_crt(int64_t p, int64_t r, int s, const CrtConsts& cc, const u
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   crt_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -547,6 +547,7 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(kp.units, g.num_sms);
   kern<<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM, st>>>(ta, tb, kp);
+  count_launches(1);
   return cudaGetLastError();
 }
 

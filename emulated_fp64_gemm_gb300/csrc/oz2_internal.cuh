@@ -66,6 +66,9 @@ const HostConsts* host_consts(int s);
 // The greedy moduli list (20 entries).
 const int* greedy_moduli20();
 
+// Counts kernel launches (reported by ozaki2_launch_count).
+void count_launches(int n);
+
 // ---------------------------------------------------------------- launchers
 struct ScaleArgs {
   int64_t p, q, r, lda, ldb;

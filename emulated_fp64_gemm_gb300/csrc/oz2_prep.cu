@@ -532,6 +532,7 @@ cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uin
   sumsq_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB, sumB);
   fast_exp_kernel<<<static_cast<unsigned>((a.p + 255) / 256), 256, 0, st>>>(amaxA, sumA, a.p, bc, alpha);
   fast_exp_kernel<<<static_cast<unsigned>((a.r + 255) / 256), 256, 0, st>>>(amaxB, sumB, a.r, bc, beta);
+  count_launches(6);
   return cudaGetLastError();
 }
 
@@ -553,6 +554,7 @@ cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, 
       a.A, a.p, a.q, a.lda, qp, amaxA, u, Abar);
   bound_quant_cols_kernel<<<dim3(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256)), 256, 0, st>>>(
       a.B, a.q, a.r, a.ldb, qp, amaxB, v, Bbar);
+  count_launches(4);
   return cudaGetLastError();
 }
 
@@ -561,6 +563,7 @@ cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,
                                   const int32_t* v, int32_t* alpha, int32_t* beta, cudaStream_t st) {
   accu_exp_kernel<<<static_cast<unsigned>((p + 255) / 256), 256, 0, st>>>(rowkey, u, p, bc, alpha);
   accu_exp_kernel<<<static_cast<unsigned>((r + 255) / 256), 256, 0, st>>>(colkey, v, r, bc, beta);
+  count_launches(2);
   return cudaGetLastError();
 }
 
@@ -578,17 +581,20 @@ cudaError_t launch_residues(const ScaleArgs& a, int64_t qp, const ModConsts& mc,
     residue_cols_kernel<3><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
   else
     residue_cols_kernel<4><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
+  count_launches(2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_planes_to_int8(const uint16_t* planes, int64_t rows, int64_t q, int64_t qp,
                                   int s, int8_t* out, cudaStream_t st) {
   planes_to_int8_kernel<<<1024, 256, 0, st>>>(planes, rows, q, qp, s, out);
+  count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_wait_timeout_selftest(int* err, long long limit_ns, cudaStream_t st) {
   wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  count_launches(1);
   return cudaGetLastError();
 }
 

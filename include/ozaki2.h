@@ -133,6 +133,20 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
                              double* C, int64_t ldc,
                              int s, int mode, void* stream);
 
+/*
+ * Stage profiling.  After ozaki2_profile_begin(max_calls), each of the next
+ * max_calls ozaki2_dgemm calls records CUDA events at its stage boundaries
+ * (stage numbering as for ozaki2_dgemm_stages) without synchronising.
+ * ozaki2_profile_end synchronises those events, writes the per-stage
+ * milliseconds summed over the recorded calls to stage_ms_sum[0..5] and the
+ * number of recorded calls to *ncalls, and turns recording off.
+ */
+oz2_status ozaki2_profile_begin(int max_calls);
+oz2_status ozaki2_profile_end(float* stage_ms_sum, int* ncalls);
+
+/* Number of kernels this library has launched so far in this process. */
+uint64_t ozaki2_launch_count(void);
+
 /* Writes the s moduli to out[0..s-1]; returns s, or -1 if s is out of range. */
 int ozaki2_moduli(int s, int32_t* out);
 
