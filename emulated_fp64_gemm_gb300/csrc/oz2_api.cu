@@ -618,6 +618,7 @@ const char* ozaki2_status_string(oz2_status status) {
     case OZ2_ERR_CUDA: return "CUDA error";
     case OZ2_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case OZ2_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+    case OZ2_ERR_SCRATCH_TOO_SMALL: return "problem exceeds the fixed no-allocation scratch";
   }
   return "unknown status";
 }

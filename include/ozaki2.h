@@ -59,7 +59,8 @@ typedef enum {
   OZ2_ERR_NO_MEMORY = 3,         /* workspace allocation failed */
   OZ2_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
   OZ2_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait gave up */
-  OZ2_ERR_UNSUPPORTED_DEVICE = 6 /* the current device is not sm_103 */
+  OZ2_ERR_UNSUPPORTED_DEVICE = 6, /* the current device is not sm_103 */
+  OZ2_ERR_SCRATCH_TOO_SMALL = 7   /* p + r exceeds OZ2_NOALLOC_MAX_VECTORS */
 } oz2_status;
 
 /* Smallest and largest number of moduli accepted. */
@@ -146,6 +147,39 @@ oz2_status ozaki2_profile_end(float* stage_ms_sum, int* ncalls);
 
 /* Number of kernels this library has launched so far in this process. */
 uint64_t ozaki2_launch_count(void);
+
+/* Largest p + r that ozaki2_fast_exponents_noalloc accepts (16 MiB of scratch). */
+#define OZ2_NOALLOC_MAX_VECTORS (1 << 20)
+
+/*
+ * Fast-mode exponents without any device allocation.  The paper has no
+ * counterpart: this entry point exists for callers that must not allocate
+ * device memory themselves or through the library, such as frameworks that
+ * hand out all device memory from their own pool, latency-critical loops
+ * where cudaMalloc could block or synchronise, and plug-ins that are not
+ * allowed to use the allocator.
+ *
+ * Computes alpha[p] and beta[r], the row and column exponents that
+ * ozaki2_dgemm uses in OZ2_FAST mode for the same A, B and s (see
+ * ozaki2_dgemm_debug), enqueued on `stream`.  A, B, alpha and beta are
+ * caller-owned device memory, layouts as for ozaki2_dgemm.
+ *
+ * Scratch: a fixed array of 2 * OZ2_NOALLOC_MAX_VECTORS 64-bit words inside
+ * the library, resident on every device that loads the library until the
+ * process exits.  Calls with p + r > OZ2_NOALLOC_MAX_VECTORS return
+ * OZ2_ERR_SCRATCH_TOO_SMALL before enqueuing anything.  Every call shares
+ * that array and clears the part it uses; calls whose kernels overlap on the
+ * GPU (e.g. on unordered streams) race on it and give wrong exponents.
+ *
+ * The first call on each device looks up the array's device address (this
+ * may load the library's device code on that device); make that first call
+ * before any stream capture.  No call allocates device memory.
+ */
+oz2_status ozaki2_fast_exponents_noalloc(int64_t p, int64_t q, int64_t r,
+                                         const double* A, int64_t lda,
+                                         const double* B, int64_t ldb,
+                                         int s, int32_t* alpha, int32_t* beta,
+                                         void* stream);
 
 /* Writes the s moduli to out[0..s-1]; returns s, or -1 if s is out of range. */
 int ozaki2_moduli(int s, int32_t* out);
