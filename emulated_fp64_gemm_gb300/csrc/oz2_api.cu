@@ -141,15 +141,10 @@ const Tables& tables() {
       Big Mh = M;
       big_divmod_small(Mh, 2);
       for (int k = 0; k < kLimbs; ++k) cc.Mhalf[k] = Mh.l[k];
-      int top = 0;
-      for (int k = kLimbs - 1; k >= 0; --k)
-        if (M.l[k]) {
-          top = k;
-          break;
-        }
-      if (top < 1) top = 1;
-      cc.top = top;
-      const double mtop = static_cast<double>(M.l[top]) * 4294967296.0 + static_cast<double>(M.l[top - 1]);
+      const int nl = crt_limbs(s);
+      cc.top = nl - 1;
+      const double mtop = static_cast<double>(M.l[nl - 1]) + static_cast<double>(M.l[nl - 2]) * 0x1p-32 +
+                          static_cast<double>(M.l[nl - 3]) * 0x1p-64;
       cc.inv_Mtop = static_cast<float>(1.0 / mtop);
       // L = M/2 - 1
       Big L = Mh;

@@ -13,173 +13,186 @@
 namespace oz2 {
 namespace {
 
-// Bits [pos, pos + 64) of a 160-bit magnitude (pos >= 0; zeros above).
-__device__ __forceinline__ uint64_t bits_at(const uint32_t (&x)[kLimbs], int pos) {
-  uint64_t r = 0;
+// Exact CRT of one output entry from its s residues (byte lanes of rv across
+// VEC entries), accumulated in 64-bit sums of 32-bit limbs.  NL limbs hold
+// every sum_t w_t M/m_t (< s M); MAXS bounds s at compile time so the
+// channel loop unrolls and every constant is an immediate operand.
+template <int NL>
+__device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConsts& cc, int k,
+                                             uint64_t* xo) {
+  uint32_t Y[NL];
+  uint64_t carry = 0;
 #pragma unroll
-  for (int k = 0; k < kLimbs; ++k) {
-    const int d = 32 * k - pos;
-    const uint64_t v = x[k];
-    if (d >= 0) {
-      if (d < 64) r |= v << d;
-    } else if (d > -32) {
-      r |= v >> (-d);
+  for (int l = 0; l < NL; ++l) {
+    const uint64_t t = acc[l] + carry;
+    Y[l] = static_cast<uint32_t>(t);
+    carry = t >> 32;
+  }
+  // quotient estimate from the top three limbs scaled as a float (the
+  // dropped limbs change Y/M by far less than the float rounding; an estimate
+  // one off is corrected exactly below)
+  const float yf = static_cast<float>(Y[NL - 1]) + static_cast<float>(Y[NL - 2]) * 0x1p-32f +
+                   static_cast<float>(Y[NL - 3]) * 0x1p-64f;
+  const int kq = static_cast<int>(floorf(yf * cc.inv_Mtop + 0.5f));
+  uint32_t X[NL];
+  {
+    int64_t c = 0;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const int64_t t = static_cast<int64_t>(Y[l]) - static_cast<int64_t>(kq) * cc.M[l] + c;
+      X[l] = static_cast<uint32_t>(t);
+      c = t >> 32;
     }
   }
-  return r;
-}
-
-// Any bit set in positions [0, b)?
-__device__ __forceinline__ bool sticky_below(const uint32_t (&x)[kLimbs], int b) {
-  bool s = false;
+  // exact correction into [-M/2, M/2): compare the top 64 bits, full compare on a tie
+  {
+    const int64_t xt = static_cast<int64_t>((static_cast<uint64_t>(X[NL - 1]) << 32) | X[NL - 2]);
+    const int64_t ht = static_cast<int64_t>((static_cast<uint64_t>(cc.Mhalf[NL - 1]) << 32) | cc.Mhalf[NL - 2]);
+    int fix = 0;
+    if (xt > ht) fix = -1;
+    else if (xt < -ht - 1) fix = 1;
+    else if (xt == ht || xt == -ht - 1) {
+      // tie on the top limbs: decide with all limbs (X >= M/2 or X < -M/2)
+      int64_t c = 0;
+      uint32_t top = 0;
 #pragma unroll
-  for (int k = 0; k < kLimbs; ++k) {
-    const int lo = 32 * k;
-    if (lo + 32 <= b) {
-      s |= x[k] != 0;
-    } else if (lo < b) {
-      s |= (x[k] & ((1u << (b - lo)) - 1u)) != 0;
+      for (int l = 0; l < NL; ++l) {
+        const int64_t t = static_cast<int64_t>(X[l]) - static_cast<int64_t>(cc.Mhalf[l]) + c;
+        top = static_cast<uint32_t>(t);
+        c = t >> 32;
+      }
+      if (static_cast<int32_t>(top) >= 0) fix = -1;
+      c = 0;
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const int64_t t = static_cast<int64_t>(X[l]) + static_cast<int64_t>(cc.Mhalf[l]) + c;
+        top = static_cast<uint32_t>(t);
+        c = t >> 32;
+      }
+      if (static_cast<int32_t>(top) < 0) fix = 1;
+    }
+    if (fix) {
+      int64_t c = 0;
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const int64_t t = static_cast<int64_t>(X[l]) + fix * static_cast<int64_t>(cc.M[l]) + c;
+        X[l] = static_cast<uint32_t>(t);
+        c = t >> 32;
+      }
     }
   }
-  return s;
-}
-
-// RN_even(sign * mag * 2^-k) as a double, subnormals and overflow included.
-__device__ __forceinline__ double round_scaled(const uint32_t (&mag)[kLimbs], bool neg, int k) {
-  int nb = 0;
+  const bool neg = static_cast<int32_t>(X[NL - 1]) < 0;
+  if (xo) {
+    uint32_t ext[6];
 #pragma unroll
-  for (int i = 0; i < kLimbs; ++i)
-    if (mag[i]) nb = 32 * i + (32 - __clz(static_cast<int>(mag[i])));
-  if (nb == 0) return 0.0;
-  int sh = nb - 53;                  // drop this many low bits for 53 significant bits
-  if (k - 1074 > sh) sh = k - 1074;  // ... or more, below the subnormal threshold
+    for (int l = 0; l < 6; ++l) ext[l] = (l < NL) ? X[l] : (neg ? 0xFFFFFFFFu : 0u);
+    xo[0] = (static_cast<uint64_t>(ext[1]) << 32) | ext[0];
+    xo[1] = (static_cast<uint64_t>(ext[3]) << 32) | ext[2];
+    xo[2] = (static_cast<uint64_t>(ext[5]) << 32) | ext[4];
+  }
+  // magnitude
+  uint32_t mag[NL];
+  {
+    uint64_t c = neg ? 1u : 0u;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t t = static_cast<uint64_t>(neg ? ~X[l] : X[l]) + c;
+      mag[l] = static_cast<uint32_t>(t);
+      c = t >> 32;
+    }
+  }
+  // move the top nonzero limb to position NL-1
+  int drop = 0;  // limbs shifted in from below
+#pragma unroll
+  for (int st = 0; st < NL - 1; ++st) {
+    if (mag[NL - 1] == 0) {
+#pragma unroll
+      for (int l = NL - 1; l > 0; --l) mag[l] = mag[l - 1];
+      mag[0] = 0;
+      ++drop;
+    }
+  }
+  if (mag[NL - 1] == 0) return 0.0;
+  const int lz = __clz(static_cast<int>(mag[NL - 1]));
+  const uint64_t hi = (static_cast<uint64_t>(mag[NL - 1]) << 32) | mag[NL - 2];
+  const uint32_t l3 = mag[NL - 3];
+  const uint64_t T = lz ? ((hi << lz) | (l3 >> (32 - lz))) : hi;  // top 64 bits, MSB at 63
+  bool sticky = lz ? ((l3 << lz) != 0) : (l3 != 0);
+#pragma unroll
+  for (int l = 0; l < NL - 3; ++l) sticky |= mag[l] != 0;
+  const int nb = 32 * (NL - drop) - lz;  // bit length of |X|
+  int E = nb - 1 - k;                     // |X| 2^-k in [2^E, 2^(E+1))
+  int d = 11;                             // bits of T dropped for 53 significant bits
+  if (E < -1022) d += -1022 - E;          // subnormal result: drop more
   uint64_t m;
-  if (sh <= 0) {
-    m = bits_at(mag, 0) << (-sh);    // exact: mag < 2^53 here
+  bool rnd, st;
+  if (d < 64) {
+    m = T >> d;
+    rnd = (T >> (d - 1)) & 1ull;
+    st = sticky || (T & ((1ull << (d - 1)) - 1ull)) != 0;
   } else {
-    const uint64_t q = bits_at(mag, sh);
-    const bool rnd = (bits_at(mag, sh - 1) & 1ull) != 0;
-    const bool st = sticky_below(mag, sh - 1);
-    m = q + ((rnd && (st || (q & 1ull))) ? 1ull : 0ull);
-    if (m == (1ull << 53)) {
-      m = 1ull << 52;
-      ++sh;
-    }
+    m = 0;
+    rnd = (d == 64) ? (T >> 63) != 0 : false;
+    st = sticky || (d == 64 ? (T & ~(1ull << 63)) != 0 : T != 0);
   }
+  m += (rnd && (st || (m & 1ull))) ? 1ull : 0ull;
   uint64_t bits;
-  if (m >= (1ull << 52)) {
-    const int biased = sh - k + 1075;
-    if (biased >= 2047) bits = 0x7FF0000000000000ull;
-    else bits = (static_cast<uint64_t>(biased) << 52) | (m & ((1ull << 52) - 1));
+  if (E >= -1022) {
+    if (m == (1ull << 53)) {
+      m >>= 1;
+      ++E;
+    }
+    bits = (E + 1023 >= 2047) ? 0x7FF0000000000000ull
+                              : ((static_cast<uint64_t>(E + 1023) << 52) | (m & ((1ull << 52) - 1)));
   } else {
-    bits = m;  // subnormal (sh == k - 1074)
+    bits = m;  // subnormal, or the smallest normal when rounding carried into bit 52
   }
   if (neg) bits |= 1ull << 63;
   return __longlong_as_double(static_cast<long long>(bits));
 }
 
-// X >= y for X signed (top limb two's complement) and y a nonnegative constant?
-__device__ __forceinline__ bool ge_const(const uint32_t (&X)[kLimbs], const uint32_t (&y)[kLimbs]) {
-  int64_t c = 0;
-#pragma unroll
-  for (int k = 0; k < kLimbs - 1; ++k) {
-    const int64_t t = static_cast<int64_t>(X[k]) - static_cast<int64_t>(y[k]) + c;
-    c = t >> 32;
-  }
-  const int64_t top = static_cast<int64_t>(static_cast<int32_t>(X[kLimbs - 1])) -
-                      static_cast<int64_t>(y[kLimbs - 1]) + c;
-  return top >= 0;
-}
-
-// X += f * y (f in {-1, +1}), y a nonnegative constant.
-__device__ __forceinline__ void add_scaled(uint32_t (&X)[kLimbs], const uint32_t (&y)[kLimbs], int f) {
-  int64_t c = 0;
-#pragma unroll
-  for (int k = 0; k < kLimbs; ++k) {
-    const int64_t t = static_cast<int64_t>(X[k]) + f * static_cast<int64_t>(y[k]) + c;
-    X[k] = static_cast<uint32_t>(t);
-    c = t >> 32;
-  }
-}
-
+template <int MAXS, int NL, int VEC>
 __global__ void __launch_bounds__(256) crt_kernel(int64_t p, int64_t r, const __grid_constant__ CrtConsts cc,
                                                   const uint8_t* __restrict__ R,
                                                   const int32_t* __restrict__ alpha,
                                                   const int32_t* __restrict__ beta,
                                                   double* __restrict__ C, int64_t ldc,
                                                   uint64_t* __restrict__ Xout) {
-  const int64_t n = p * r;
+  const int64_t pv = p / VEC;
+  const int64_t groups = pv * r;
   const int64_t plane = p * r;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t i = idx % p;
-    const int64_t j = idx / p;
-    const uint8_t* Rp = R + idx;  // R_t[j][i] = R[t * plane + j * p + i]
-    uint64_t acc[kLimbs] = {0, 0, 0, 0, 0};
-    for (int t = 0; t < cc.s; ++t) {
-      const uint32_t m = static_cast<uint32_t>(cc.m[t]);
-      const uint32_t x = static_cast<uint32_t>(Rp[t * plane]) * cc.inv[t];  // < 2^16
-      const uint32_t w = x - __umulhi(x, cc.magic32[t]) * m;                   // x mod m
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t j = g / pv;
+    const int64_t i0 = (g - j * pv) * VEC;
+    const int64_t base = j * p + i0;
+    uint64_t acc[VEC][NL];
 #pragma unroll
-      for (int k = 0; k < kLimbs; ++k) acc[k] += static_cast<uint64_t>(w) * cc.Mt[t][k];
-    }
-    uint32_t Y[kLimbs];
-    uint64_t carry = 0;
+    for (int v = 0; v < VEC; ++v)
 #pragma unroll
-    for (int k = 0; k < kLimbs; ++k) {
-      const uint64_t t = acc[k] + carry;
-      Y[k] = static_cast<uint32_t>(t);
-      carry = t >> 32;
-    }
-    // k = round(Y / M) from the top limbs (exactly corrected below)
-    float yf = 0.0f;
-    {
-      const int top = cc.top;
-      const float y2 = (top + 1 < kLimbs) ? static_cast<float>(Y[top + 1]) : 0.0f;
-      yf = (y2 * 4294967296.0f + static_cast<float>(Y[top])) * 4294967296.0f +
-           static_cast<float>(Y[top - 1]);
-    }
-    const int kq = static_cast<int>(floorf(yf * cc.inv_Mtop + 0.5f));
-    uint32_t X[kLimbs];
-    {
-      int64_t c = 0;
+      for (int l = 0; l < NL; ++l) acc[v][l] = 0;
 #pragma unroll
-      for (int k = 0; k < kLimbs; ++k) {
-        const int64_t t = static_cast<int64_t>(Y[k]) - static_cast<int64_t>(kq) * cc.M[k] + c;
-        X[k] = static_cast<uint32_t>(t);
-        c = t >> 32;
+    for (int t = 0; t < MAXS; ++t) {
+      if (t < cc.s) {
+        uint32_t rv;
+        if (VEC == 4) rv = __ldg(reinterpret_cast<const uint32_t*>(R + t * plane + base));
+        else rv = __ldg(R + t * plane + base);
+        const uint32_t m = static_cast<uint32_t>(cc.m[t]);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+          const uint32_t x = ((rv >> (8 * v)) & 255u) * cc.inv[t];  // < 2^16
+          const uint32_t w = x - __umulhi(x, cc.magic32[t]) * m;   // x mod m
+#pragma unroll
+          for (int l = 0; l < NL; ++l) acc[v][l] += static_cast<uint64_t>(w) * cc.Mt[t][l];
+        }
       }
     }
-    if (ge_const(X, cc.Mhalf)) add_scaled(X, cc.M, -1);  // X >= M/2: subtract M
-    // X < -M/2  <=>  X + M/2 < 0
-    {
-      uint32_t Z[kLimbs];
+    const int bj = beta[j];
 #pragma unroll
-      for (int k = 0; k < kLimbs; ++k) Z[k] = X[k];
-      add_scaled(Z, cc.Mhalf, 1);
-      if (static_cast<int32_t>(Z[kLimbs - 1]) < 0) add_scaled(X, cc.M, 1);
+    for (int v = 0; v < VEC; ++v) {
+      const int64_t i = i0 + v;
+      C[j * ldc + i] = crt_finish<NL>(acc[v], cc, alpha[i] + bj, Xout ? Xout + (base + v) * 3 : nullptr);
     }
-    const bool neg = static_cast<int32_t>(X[kLimbs - 1]) < 0;
-    if (Xout) {
-      uint64_t* xo = Xout + idx * 3;
-      xo[0] = (static_cast<uint64_t>(X[1]) << 32) | X[0];
-      xo[1] = (static_cast<uint64_t>(X[3]) << 32) | X[2];
-      xo[2] = static_cast<uint64_t>(static_cast<int64_t>(static_cast<int32_t>(X[4])));
-    }
-    uint32_t mag[kLimbs];
-    if (neg) {
-      uint64_t c = 1;
-#pragma unroll
-      for (int k = 0; k < kLimbs; ++k) {
-        const uint64_t t = static_cast<uint64_t>(~X[k]) + c;
-        mag[k] = static_cast<uint32_t>(t);
-        c = t >> 32;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kLimbs; ++k) mag[k] = X[k];
-    }
-    C[j * ldc + i] = round_scaled(mag, neg, alpha[i] + beta[j]);
   }
 }
 
@@ -188,16 +201,27 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t p, int64_t r, const __
 cudaError_t launch_crt(int64_t p, int64_t r, int s, const CrtConsts& cc, const uint8_t* R,
                        const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
                        uint64_t* X, cudaStream_t st) {
-  (void)s;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t n = p * r;
-  int64_t blocks = (n + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  const bool vec = (p % 4) == 0;
+  const int64_t groups = (vec ? p / 4 : p) * r;
+  int64_t blocks = (groups + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  crt_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  const unsigned b = static_cast<unsigned>(blocks);
+  // limbs needed for sum_t w_t M/m_t < s M: 3 for s <= 11, 4 for s <= 15, 5 up to 20
+  if (crt_limbs(s) == 3) {
+    if (vec) crt_kernel<11, 3, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+    else crt_kernel<11, 3, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  } else if (crt_limbs(s) == 4) {
+    if (vec) crt_kernel<15, 4, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+    else crt_kernel<15, 4, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  } else {
+    if (vec) crt_kernel<20, 5, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+    else crt_kernel<20, 5, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

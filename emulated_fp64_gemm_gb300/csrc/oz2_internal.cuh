@@ -46,9 +46,13 @@ struct CrtConsts {  // per-s CRT constants
   uint32_t Mt[kSMax][kLimbs];     // M/m_t, little-endian 32-bit limbs
   uint32_t M[kLimbs];             // M
   uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
-  int top;                        // index of the top nonzero limb of M (>= 1)
-  float inv_Mtop;                 // 1 / (M_top64 as float), for the quotient estimate
+  int top;                        // NL - 1: the top limb of the CRT kernel's sums
+  float inv_Mtop;                 // 1 / (M[NL-1] + M[NL-2] 2^-32 + M[NL-3] 2^-64)
 };
+
+// 32-bit limbs the CRT kernel uses for sum_t w_t M/m_t < s M: enough for
+// bits(M) + 5 bits (s <= 20 < 2^5).  3 for s <= 11, 4 for s <= 15, 5 above.
+inline int crt_limbs(int s) { return s <= 11 ? 3 : (s <= 15 ? 4 : 5); }
 
 struct BoundConsts {  // L = M/2 - 1 in the form the exponent kernels compare against
   int Lbits;                      // bit length of L
