@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -177,9 +178,17 @@ struct DeviceState {
   bool supported = false;
 };
 
+constexpr int kMaxBlocks = 8;  // row blocks of the overlapped schedule
+
 struct Workspace {
   size_t bytes = 0;
   uint8_t* base = nullptr;
+  // second stream and events of the overlapped schedule (created on first use)
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_ready = nullptr;
+  cudaEvent_t ev_res[kMaxBlocks] = {};
+  cudaEvent_t ev_gemm[kMaxBlocks] = {};
+  cudaEvent_t ev_done = nullptr;
 };
 
 std::mutex g_mutex;
@@ -259,10 +268,20 @@ Layout make_layout(int64_t p, int64_t q, int64_t r, int s, int64_t qp, bool stag
   return L;
 }
 
-oz2_status get_workspace(cudaStream_t st, size_t bytes, uint8_t** base) {
+oz2_status workspace_sync_objects(Workspace& w) {
+  if (w.aux) return OZ2_OK;
+  if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
+  auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done);
+  for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_gemm[b]);
+  return ok ? OZ2_OK : OZ2_ERR_CUDA;
+}
+
+oz2_status get_workspace(cudaStream_t st, size_t bytes, uint8_t** base, Workspace** wout = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ2_ERR_CUDA;
   Workspace& w = g_ws[std::make_pair(dev, st)];
+  if (wout) *wout = &w;
   if (w.bytes < bytes) {
     if (w.base) {
       cudaDeviceSynchronize();
@@ -313,7 +332,7 @@ struct Outputs {  // optional checking outputs
 oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
                         const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
                         cudaStream_t st, const Outputs* dbg, cudaEvent_t* ev, uint8_t** ws_out,
-                        Layout* lay_out) {
+                        Layout* lay_out, bool pipelined) {
   DeviceState* ds = nullptr;
   oz2_status e = device_state(&ds);
   if (e != OZ2_OK) return e;
@@ -321,7 +340,8 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   const int64_t qp = (q + kKPad - 1) / kKPad * kKPad;
   const Layout L = make_layout(p, q, r, s, qp, lay_out != nullptr);
   uint8_t* ws = nullptr;
-  e = get_workspace(st, L.total, &ws);
+  Workspace* wsp = nullptr;
+  e = get_workspace(st, L.total, &ws, &wsp);
   if (e != OZ2_OK) return e;
   if (ws_out) *ws_out = ws;
   if (lay_out) *lay_out = L;
@@ -373,25 +393,68 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   }
   // |trunc(2^alpha a)| <= sqrt(L) in fast mode; accu entries beyond the limbs take the general path
   const int max_bits = (hc->bound.Lbits + 1) / 2;
-  OZ2_CU(launch_residues(sa, qp, hc->mod, alpha, beta, ds->pow2mod, max_bits, max_bits, planesA,
-                         planesB, st));
-  if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
-  {
-    GemmArgs g{};
+  GemmArgs g{};
+  g.r = r;
+  g.qp = qp;
+  g.s = s;
+  g.p_total = p;
+  g.Aplanes = planesA;
+  g.Bplanes = planesB;
+  g.R = Rw;
+  g.err = ds->err;
+  g.num_sms = ds->num_sms;
+  // Row blocks of the overlapped schedule: residues of block b+1 and the CRT
+  // of block b run on a second stream while the tensor cores work on the
+  // GEMMs of block b (the grouped-overlap idea of the profiling study, §10.2,
+  // applied to row blocks so that the CRT overlaps too).
+  int64_t block_rows = (p + 3) / 4;
+  block_rows = (block_rows + 127) / 128 * 128;
+  if (block_rows < 1024) block_rows = 1024;
+  const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
+  const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;
+  if (!overlap) {
+    OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
+    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
     g.p = p;
-    g.r = r;
-    g.qp = qp;
-    g.s = s;
-    g.Aplanes = planesA;
-    g.Bplanes = planesB;
-    g.R = Rw;
-    g.err = ds->err;
-    g.num_sms = ds->num_sms;
+    g.row0 = 0;
     OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
+    OZ2_CU(launch_crt(0, p, p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
+  } else {
+    e = workspace_sync_objects(*wsp);
+    if (e != OZ2_OK) return e;
+    cudaStream_t aux = wsp->aux;
+    auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
+    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+    OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
+                                planesA, st));
+    OZ2_CU(cudaEventRecord(wsp->ev_ready, st));
+    OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
+    for (int b = 1; b < nb; ++b) {
+      const int64_t r0 = b * block_rows;
+      OZ2_CU(launch_residues_rows(A + r0, rows_of(b), q, lda, qp, p, hc->mod, alpha + r0, ds->pow2mod,
+                                  max_bits, planesA + r0 * qp, aux));
+      OZ2_CU(cudaEventRecord(wsp->ev_res[b], aux));
+    }
+    if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
+    for (int b = 0; b < nb; ++b) {
+      if (b > 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
+      g.row0 = b * block_rows;
+      g.p = rows_of(b);
+      OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
+      OZ2_CU(cudaEventRecord(wsp->ev_gemm[b], st));
+    }
+    if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
+    for (int b = 0; b < nb; ++b) {
+      OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_gemm[b], 0));
+      OZ2_CU(launch_crt(b * block_rows, rows_of(b), p, r, s, hc->crt, Rw, alpha, beta, C, ldc, nullptr, aux));
+    }
+    OZ2_CU(cudaEventRecord(wsp->ev_done, aux));
+    OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_done, 0));
+    if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
   }
-  if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
-  OZ2_CU(launch_crt(p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
-  if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
 
   if (dbg) {
     if (dbg->alpha) OZ2_CU(cudaMemcpyAsync(dbg->alpha, alpha, p * 4, cudaMemcpyDeviceToDevice, st));
@@ -443,7 +506,7 @@ oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r, const double* A, int64_
   cudaEvent_t* ev = nullptr;
   if (g_prof.on && g_prof.used < g_prof.max_calls) ev = &g_prof.ev[static_cast<size_t>(g_prof.used++) * 6];
   return run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, static_cast<cudaStream_t>(stream),
-                      nullptr, ev, nullptr, nullptr);
+                      nullptr, ev, nullptr, nullptr, true);
 }
 
 oz2_status ozaki2_profile_begin(int max_calls) {
@@ -505,7 +568,7 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, 
   o.R = R;
   o.X = X;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, &o, nullptr, nullptr, nullptr);
+  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, &o, nullptr, nullptr, nullptr, false);
   if (e != OZ2_OK) return e;
   if (cudaStreamSynchronize(st) != cudaSuccess) return OZ2_ERR_CUDA;
   return OZ2_OK;
@@ -522,7 +585,7 @@ oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r, const double* A,
   cudaEvent_t ev[6];
   for (auto& x : ev)
     if (cudaEventCreate(&x) != cudaSuccess) return OZ2_ERR_CUDA;
-  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, nullptr, ev, nullptr, nullptr);
+  e = run_pipeline(p, q, r, A, lda, B, ldb, C, ldc, s, mode, st, nullptr, ev, nullptr, nullptr, false);
   if (e == OZ2_OK) {
     if (cudaEventSynchronize(ev[5]) != cudaSuccess) e = OZ2_ERR_CUDA;
     for (int k = 0; k < 5 && e == OZ2_OK; ++k) cudaEventElapsedTime(&stage_ms[k], ev[k], ev[k + 1]);
@@ -553,7 +616,7 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r, const double* A, i
   OZ2_CU(cudaMemcpy2DAsync(dA, p * 8, A, lda * 8, p * 8, q, cudaMemcpyHostToDevice, st));
   OZ2_CU(cudaMemcpy2DAsync(dB, q * 8, B, ldb * 8, q * 8, r, cudaMemcpyHostToDevice, st));
   Layout L2;
-  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2);
+  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2, true);
   if (e != OZ2_OK) return e;
   OZ2_CU(cudaMemcpy2DAsync(C, ldc * 8, dC, p * 8, p * 8, r, cudaMemcpyDeviceToHost, st));
   OZ2_CU(cudaStreamSynchronize(st));

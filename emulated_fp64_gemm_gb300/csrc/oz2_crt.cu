@@ -151,21 +151,23 @@ __device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConst
   return __longlong_as_double(static_cast<long long>(bits));
 }
 
+// Output rows [row0, row0 + rows); R and X have p_total rows per column.
 template <int MAXS, int NL, int VEC>
-__global__ void __launch_bounds__(256) crt_kernel(int64_t p, int64_t r, const __grid_constant__ CrtConsts cc,
+__global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total, int64_t r,
+                                                  const __grid_constant__ CrtConsts cc,
                                                   const uint8_t* __restrict__ R,
                                                   const int32_t* __restrict__ alpha,
                                                   const int32_t* __restrict__ beta,
                                                   double* __restrict__ C, int64_t ldc,
                                                   uint64_t* __restrict__ Xout) {
-  const int64_t pv = p / VEC;
+  const int64_t pv = rows / VEC;
   const int64_t groups = pv * r;
-  const int64_t plane = p * r;
+  const int64_t plane = p_total * r;
   for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t j = g / pv;
-    const int64_t i0 = (g - j * pv) * VEC;
-    const int64_t base = j * p + i0;
+    const int64_t i0 = row0 + (g - j * pv) * VEC;
+    const int64_t base = j * p_total + i0;
     uint64_t acc[VEC][NL];
 #pragma unroll
     for (int v = 0; v < VEC; ++v)
@@ -198,30 +200,33 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t p, int64_t r, const __
 
 }  // namespace
 
-cudaError_t launch_crt(int64_t p, int64_t r, int s, const CrtConsts& cc, const uint8_t* R,
-                       const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
-                       uint64_t* X, cudaStream_t st) {
+cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, int s,
+                       const CrtConsts& cc, const uint8_t* R, const int32_t* alpha,
+                       const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bool vec = (p % 4) == 0;
-  const int64_t groups = (vec ? p / 4 : p) * r;
+  const bool vec = (rows % 4) == 0 && (row0 % 4) == 0 && (p_total % 4) == 0;
+  const int64_t groups = (vec ? rows / 4 : rows) * r;
   int64_t blocks = (groups + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const unsigned b = static_cast<unsigned>(blocks);
-  // limbs needed for sum_t w_t M/m_t < s M: 3 for s <= 11, 4 for s <= 15, 5 up to 20
-  if (crt_limbs(s) == 3) {
-    if (vec) crt_kernel<11, 3, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
-    else crt_kernel<11, 3, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
-  } else if (crt_limbs(s) == 4) {
-    if (vec) crt_kernel<15, 4, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
-    else crt_kernel<15, 4, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+  const int nl = crt_limbs(s);
+#define OZ2_CRT_LAUNCH(MS, NLV, V) \
+  crt_kernel<MS, NLV, V><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, R, alpha, beta, C, ldc, X)
+  if (nl == 3) {
+    if (vec) OZ2_CRT_LAUNCH(11, 3, 4);
+    else OZ2_CRT_LAUNCH(11, 3, 1);
+  } else if (nl == 4) {
+    if (vec) OZ2_CRT_LAUNCH(15, 4, 4);
+    else OZ2_CRT_LAUNCH(15, 4, 1);
   } else {
-    if (vec) crt_kernel<20, 5, 4><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
-    else crt_kernel<20, 5, 1><<<b, 256, 0, st>>>(p, r, cc, R, alpha, beta, C, ldc, X);
+    if (vec) OZ2_CRT_LAUNCH(20, 5, 4);
+    else OZ2_CRT_LAUNCH(20, 5, 1);
   }
+#undef OZ2_CRT_LAUNCH
   count_launches(1);
   return cudaGetLastError();
 }

@@ -56,7 +56,9 @@ struct Cfg {
 };
 
 struct KParams {
-  int64_t p, r;
+  int64_t p, r;     // output rows of this launch, output columns
+  int64_t row0;     // first output row (and row of A's planes) of this launch
+  int64_t p_total;  // rows of R / P (their column stride)
   int s;
   int nkb;          // K blocks (qp / 64)
   int nchunks;      // ceil(nkb / KC_BLOCKS)
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               const uint32_t fb = smem_u32(&full[stage]);
               mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-              tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK, U.tm * BM, U.t, fb);
+              tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK,
+                          static_cast<int>(kp.row0) + U.tm * BM, U.t, fb);
               tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK, (U.tn0 + sl) * BN, U.t, fb);
               ++issued;
               if (++stage == C::STAGES) {
@@ -345,7 +348,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
       const Unit U = decode_unit(u, kp);
-      const int64_t i = static_cast<int64_t>(U.tm) * BM + row_in_tile;
+      const int64_t il = static_cast<int64_t>(U.tm) * BM + row_in_tile;  // row within this launch
+      const int64_t i = kp.row0 + il;                                       // global row
       const float mf = kp.mf[U.t];
       const float inv_m = kp.inv_mf[U.t];
       for (int c = 0; c < kp.nchunks && ok; ++c) {
@@ -381,13 +385,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_wait_st();
             } else {
               // final: R = D mod m in [0, m)
-              uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p * kp.r;
+              uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
 #pragma unroll 1
               for (int cb = 0; cb < BN / 32; ++cb) {
                 uint32_t v[32];
                 tmem_ld32(acc_addr + cb * 32, v);
                 tmem_wait_ld();
-                if (i < kp.p) {
+                if (il < kp.p) {
 #pragma unroll
                   for (int k = 0; k < 32; ++k) {
                     const int64_t j = j0 + cb * 32 + k;
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
                     float rr = fmaf(-mf, q, d);
                     rr = (rr < 0.0f) ? rr + mf : rr;
-                    if (j < kp.r) Rt[j * kp.p + i] = static_cast<uint8_t>(__float2uint_rn(rr));
+                    if (j < kp.r) Rt[j * kp.p_total + i] = static_cast<uint8_t>(__float2uint_rn(rr));
                   }
                 }
               }
@@ -418,22 +422,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (!last) {
                 tmem_st32(sum_addr + cb * 32, sacc);
               } else if (KIND == kGemmExactP) {
-                int32_t* Pt = kp.P + static_cast<int64_t>(U.t) * kp.p * kp.r;
-                if (i < kp.p) {
+                int32_t* Pt = kp.P + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
+                if (il < kp.p) {
 #pragma unroll
                   for (int k = 0; k < 32; ++k) {
                     const int64_t j = j0 + cb * 32 + k;
-                    if (j < kp.r) Pt[j * kp.p + i] = static_cast<int32_t>(sacc[k]);
+                    if (j < kp.r) Pt[j * kp.p_total + i] = static_cast<int32_t>(sacc[k]);
                   }
                 }
               } else {
                 // kGemmBound: row max of W 2^-v_j, column max of W 2^-u_i
-                const int ui = (i < kp.p) ? kp.u[i] : 0;
+                const int ui = (il < kp.p) ? kp.u[i] : 0;
                 uint64_t rmax = 0;
 #pragma unroll 4
                 for (int k = 0; k < 32; ++k) {
                   const int64_t j = j0 + cb * 32 + k;
-                  const bool valid = (i < kp.p) && (j < kp.r);
+                  const bool valid = (il < kp.p) && (j < kp.r);
                   const uint32_t w = valid ? sacc[k] : 0u;
                   if (valid) {
                     const uint64_t kr = dyadic_key(w, kp.v[j]);
@@ -519,11 +523,14 @@ template <int BN, int KIND>
 cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
-  if (!make_plane_map(&ta, g.Aplanes, g.qp, g.p, g.s, BM)) return cudaErrorInvalidValue;
+  const int64_t p_total = g.p_total ? g.p_total : g.p;
+  if (!make_plane_map(&ta, g.Aplanes, g.qp, p_total, g.s, BM)) return cudaErrorInvalidValue;
   if (!make_plane_map(&tb, g.Bplanes, g.qp, g.r, g.s, BN)) return cudaErrorInvalidValue;
   KParams kp{};
   kp.p = g.p;
   kp.r = g.r;
+  kp.row0 = g.row0;
+  kp.p_total = p_total;
   kp.s = g.s;
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;

@@ -95,17 +95,24 @@ cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,
                                   const uint64_t* rowkey, const uint64_t* colkey, const int32_t* u,
                                   const int32_t* v, int32_t* alpha, int32_t* beta, cudaStream_t st);
 
-// residue planes: A -> [s][p][qp], B -> [s][r][qp] (fp16 values in [-128, 127]).
-cudaError_t launch_residues(const ScaleArgs& a, int64_t qp, const ModConsts& mc,
-                            const int32_t* alpha, const int32_t* beta, const uint8_t* pow2mod,
-                            int max_bits_A, int max_bits_B, uint16_t* planesA,
-                            uint16_t* planesB, cudaStream_t st);
+// residue planes of `rows` rows of A (column-major, leading dimension lda)
+// into fp16 planes [s][plane_rows][qp]; `planes` points at the first row.
+cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64_t lda, int64_t qp,
+                                 int64_t plane_rows, const ModConsts& mc, const int32_t* alpha,
+                                 const uint8_t* pow2mod, int max_bits, uint16_t* planes,
+                                 cudaStream_t st);
+// residue planes of B (column-major q x r) into fp16 planes [s][r][qp].
+cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
+                                 const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
+                                 int max_bits, uint16_t* planes, cudaStream_t st);
 
 // GEMM epilogue kinds
 enum GemmKind { kGemmMod = 0, kGemmExactP = 1, kGemmBound = 2 };
 
 struct GemmArgs {
-  int64_t p, r, qp;       // rows of A planes, rows of B planes, padded K
+  int64_t p, r, qp;       // rows of output computed by this launch, rows of B planes, padded K
+  int64_t row0 = 0;       // first row (of A's planes and of the output) of this launch
+  int64_t p_total = 0;    // rows of A's planes and of R / P (0: same as p)
   int s;                  // number of channels (planes)
   const uint16_t* Aplanes;  // [s][p][qp]
   const uint16_t* Bplanes;  // [s][r][qp]
@@ -121,10 +128,10 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st);
 
-// CRT + inverse scaling
-cudaError_t launch_crt(int64_t p, int64_t r, int s, const CrtConsts& cc, const uint8_t* R,
-                       const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
-                       uint64_t* X, cudaStream_t st);
+// CRT + inverse scaling of output rows [row0, row0 + rows) (R, X: p_total rows)
+cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, int s,
+                       const CrtConsts& cc, const uint8_t* R, const int32_t* alpha,
+                       const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st);
 
 // debug copies
 cudaError_t launch_planes_to_int8(const uint16_t* planes, int64_t rows, int64_t q, int64_t qp,

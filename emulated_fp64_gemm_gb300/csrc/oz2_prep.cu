@@ -419,6 +419,7 @@ __device__ __forceinline__ void residues8(const double (&x)[8], int scale, const
 template <int NL>
 __global__ void __launch_bounds__(256) residue_rows_kernel(const double* __restrict__ A, int64_t p,
                                                            int64_t q, int64_t lda, int64_t qp,
+                                                           int64_t plane_rows,
                                                            const int32_t* __restrict__ alpha,
                                                            ModConsts mc,
                                                            const uint8_t* __restrict__ pow2mod,
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(256) residue_rows_kernel(const double* __restr
   double x[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
-  residues8<NL>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, p * qp);
+  residues8<NL>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, plane_rows * qp);
 }
 
 // B (column-major q x r) -> planes [s][r][qp]: one warp per column, 8
@@ -567,21 +568,28 @@ cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,
   return cudaGetLastError();
 }
 
-cudaError_t launch_residues(const ScaleArgs& a, int64_t qp, const ModConsts& mc,
-                            const int32_t* alpha, const int32_t* beta, const uint8_t* pow2mod,
-                            int max_bits_A, int max_bits_B, uint16_t* planesA, uint16_t* planesB,
-                            cudaStream_t st) {
-  const dim3 gA(static_cast<unsigned>((a.p + 31) / 32), static_cast<unsigned>(qp / 64));
-  const dim3 gB(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256));
-  if (max_bits_A <= 63)
-    residue_rows_kernel<3><<<gA, 256, 0, st>>>(a.A, a.p, a.q, a.lda, qp, alpha, mc, pow2mod, planesA);
+cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64_t lda, int64_t qp,
+                                 int64_t plane_rows, const ModConsts& mc, const int32_t* alpha,
+                                 const uint8_t* pow2mod, int max_bits, uint16_t* planes,
+                                 cudaStream_t st) {
+  const dim3 g(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(qp / 64));
+  if (max_bits <= 63)
+    residue_rows_kernel<3><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
   else
-    residue_rows_kernel<4><<<gA, 256, 0, st>>>(a.A, a.p, a.q, a.lda, qp, alpha, mc, pow2mod, planesA);
-  if (max_bits_B <= 63)
-    residue_cols_kernel<3><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
+    residue_rows_kernel<4><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
+                                 const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
+                                 int max_bits, uint16_t* planes, cudaStream_t st) {
+  const dim3 g(static_cast<unsigned>((r + 7) / 8), static_cast<unsigned>((qp + 255) / 256));
+  if (max_bits <= 63)
+    residue_cols_kernel<3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   else
-    residue_cols_kernel<4><<<gB, 256, 0, st>>>(a.B, a.q, a.r, a.ldb, qp, beta, mc, pow2mod, planesB);
-  count_launches(2);
+    residue_cols_kernel<4><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
+  count_launches(1);
   return cudaGetLastError();
 }
 

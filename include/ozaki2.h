@@ -137,7 +137,12 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
 /*
  * Stage profiling.  After ozaki2_profile_begin(max_calls), each of the next
  * max_calls ozaki2_dgemm calls records CUDA events at its stage boundaries
- * (stage numbering as for ozaki2_dgemm_stages) without synchronising.
+ * without synchronising.  ozaki2_dgemm overlaps stages (row blocks: the
+ * residues of block b+1 and the CRT of block b run on a second stream while
+ * the GEMMs of block b run on `stream`), so here stage 2 is the residue time
+ * before the first GEMM starts, stage 3 the span of all GEMM launches on
+ * `stream`, and stage 4 the CRT time after the last GEMM; stages 0, 1 and 5
+ * are as for ozaki2_dgemm_stages, which runs the stages one after another.
  * ozaki2_profile_end synchronises those events, writes the per-stage
  * milliseconds summed over the recorded calls to stage_ms_sum[0..5] and the
  * number of recorded calls to *ncalls, and turns recording off.

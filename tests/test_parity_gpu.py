@@ -207,3 +207,17 @@ def _sampled_check(oz2, name, nsamp=384):
                                   "n8192_s18_fast", "n8192_s18_accu", "p16384_q8192_r16384_s18_accu"])
 def test_full_size_workloads_sampled(oz2, name):
     _sampled_check(oz2, name)
+
+
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+def test_overlapped_row_blocks_match_sequential(oz2, mode):
+    """p = 2500 gives three row blocks (1024, 1024, 452) in the overlapped schedule."""
+    A, B = make_matrices(2500, 300, 200, 1.0, 77)
+    dA, dB = _dev(A), _dev(B)
+    got = oz2.dgemm_debug(dA, dB, 14, mode, want_p=False)  # stages one after another
+    C = oz2.dgemm(dA, dB, 14, mode)                          # overlapped row blocks
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(C.cpu().numpy(), got["C"].cpu().numpy())
+    ref = oracle.oracle_dgemm(A, B, 14, mode)
+    assert ulp_distance(C.cpu().numpy(), ref["C"]) <= ULP_TOL
+    np.testing.assert_array_equal(got["R"].cpu().numpy(), np.transpose(ref["R"], (0, 2, 1)))
