@@ -403,12 +403,14 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   g.R = Rw;
   g.err = ds->err;
   g.num_sms = ds->num_sms;
+  // CTA-pair GEMM (tcgen05 cta_group::2) unless OZ2_GEMM_1SM selects the single-SM kernel
+  g.use_2sm = std::getenv("OZ2_GEMM_1SM") == nullptr;
   // Row blocks of the overlapped schedule: residues of block b+1 and the CRT
   // of block b run on a second stream while the tensor cores work on the
   // GEMMs of block b (the grouped-overlap idea of the profiling study, §10.2,
   // applied to row blocks so that the CRT overlaps too).
   int64_t block_rows = (p + 3) / 4;
-  block_rows = (block_rows + 127) / 128 * 128;
+  block_rows = (block_rows + 255) / 256 * 256;  // whole 256-row pair tiles
   if (block_rows < 1024) block_rows = 1024;
   const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
   const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;

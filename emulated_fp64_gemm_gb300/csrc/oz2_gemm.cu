@@ -171,6 +171,12 @@ __device__ __forceinline__ uint64_t dyadic_key(uint32_t w, int x) {
   return (static_cast<uint64_t>(E + 4096) << 32) | static_cast<uint64_t>(w << (32 - b));
 }
 
+// First K block of chunk c: the nkb blocks are split into nchunks chunks of
+// equal size (+-1), each at most KC_BLOCKS long.
+__device__ __forceinline__ int chunk_begin(int c, const KParams& kp) {
+  return static_cast<int>((static_cast<int64_t>(c) * kp.nkb) / kp.nchunks);
+}
+
 // --------------------------------------------------------------------- unit decode
 struct Unit {
   int t, tm, tn0, ntile;
@@ -181,8 +187,10 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KParams& kp) {
   Unit U;
   U.t = static_cast<int>(u / upp);
   const int64_t w = u % upp;
-  // grouped raster: groups of GM row tiles, column pairs outer within a group
-  constexpr int GM = 8;
+  // grouped raster: groups of GM row tiles, column pairs outer within a group,
+  // so the ~152 units in flight cover a compact output block whose A and B
+  // tiles stay in L2 while they are reused
+  constexpr int GM = 16;
   const int64_t per_group = static_cast<int64_t>(GM) * kp.pairs_n;
   const int64_t g = w / per_group;
   const int64_t idx = w % per_group;
@@ -256,8 +264,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
         const Unit U = decode_unit(u, kp);
         for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = c * KC_BLOCKS;
-          const int kb1 = min(kb0 + KC_BLOCKS, kp.nkb);
+          const int kb0 = chunk_begin(c, kp);
+          const int kb1 = chunk_begin(c + 1, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             for (int kb = kb0; kb < kb1; ++kb) {
               if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
@@ -296,8 +304,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
         const Unit U = decode_unit(u, kp);
         for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = c * KC_BLOCKS;
-          const int kb1 = min(kb0 + KC_BLOCKS, kp.nkb);
+          const int kb0 = chunk_begin(c, kp);
+          const int kb1 = chunk_begin(c + 1, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             if (!mbar_wait_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               ok = false;
@@ -490,6 +498,349 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ====================================================================== 2-SM variant
+// A cluster of two CTAs (a CTA pair on two SMs) computes a 256 x 256 tile per
+// MMA with tcgen05.mma.cta_group::2: each CTA holds 128 rows of A and 128 of
+// the 256 rows of B^T in its own shared memory, and 128 rows x 256 columns of
+// the fp32 accumulator in its own tensor memory.  Per SM this needs 32 KB of
+// operands per 64-deep K stage instead of 48 KB, so six stages fit and the
+// pipeline covers 1.5x the load latency, and L2 reads drop by a third.
+// The leader CTA (rank 0) issues every MMA; both producers signal the
+// leader's "full" barriers, the MMA commits are multicast to both CTAs, and
+// both epilogues signal the leader's "empty accumulator" barriers.  The chunk
+// schedule and the in-place reduction are those of the single-SM kernel.
+namespace sm2 {
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB: this CTA's 128 rows of A
+constexpr int B_BYTES = 128 * BK * 2;      // 16 KB: this CTA's 128 of the 256 rows of B^T
+constexpr int STAGE_TX = 2 * (A_BYTES + B_BYTES);  // bytes landing per stage across the pair
+constexpr int GUARD = 16384;               // slack after the last B stage
+constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + GUARD + 256;
+constexpr int BN = 256;                    // output columns per tile
+}  // namespace sm2
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair
+// once every MMA issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t addr, uint32_t parity,
+                                                          volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(addr, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+struct Unit2 {
+  int t, mp, tn0, ntile;  // channel, 256-row pair tile, first 256-column tile, tiles (1 or 2)
+};
+
+__device__ __forceinline__ Unit2 decode_unit2(int64_t u, const KParams& kp) {
+  // kp.tiles_m counts 256-row pair tiles here
+  const int64_t upp = static_cast<int64_t>(kp.tiles_m) * kp.pairs_n;
+  Unit2 U;
+  U.t = static_cast<int>(u / upp);
+  const int64_t w = u % upp;
+  constexpr int GM = 8;  // 8 pair tiles = 2048 rows per raster group
+  const int64_t per_group = static_cast<int64_t>(GM) * kp.pairs_n;
+  const int64_t g = w / per_group;
+  const int64_t idx = w % per_group;
+  const int64_t left = kp.tiles_m - g * GM;
+  const int rows_in_group = static_cast<int>(left < GM ? left : GM);
+  U.mp = static_cast<int>(g * GM + idx % rows_in_group);
+  const int pn = static_cast<int>(idx / rows_in_group);
+  U.tn0 = pn * 2;
+  U.ntile = (U.tn0 + 1 < kp.tiles_n) ? 2 : 1;
+  return U;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    oz2_gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ KParams kp) {
+  using namespace sm2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES) + GUARD);
+  uint64_t* full = bars;                  // [STAGES] used in the leader only
+  uint64_t* empty = bars + STAGES;        // [STAGES] in both CTAs
+  uint64_t* accf = bars + 2 * STAGES;     // [2] in both CTAs
+  uint64_t* acce = accf + 2;              // [2] used in the leader only
+  uint64_t* drain = acce + 2;             // [1] leader
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int64_t cluster = blockIdx.x >> 1;
+  const int64_t nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&accf[i]), 1);
+      mbar_init(smem_u32(&acce[i]), 8);  // one elected lane per epilogue warp, 4 warps x 2 CTAs
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
+        const Unit2 U = decode_unit2(u, kp);
+        const int arow = static_cast<int>(kp.row0) + U.mp * 256 + static_cast<int>(rank) * 128;
+        for (int c = 0; c < kp.nchunks && ok; ++c) {
+          const int kb0 = chunk_begin(c, kp);
+          const int kb1 = chunk_begin(c + 1, kp);
+          for (int sl = 0; sl < U.ntile && ok; ++sl) {
+            const int brow = (U.tn0 + sl) * BN + static_cast<int>(rank) * 128;
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait_cluster_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb_local = smem_u32(&full[stage]);
+              const uint32_t fb_leader = map_to_rank(fb_local, 0);
+              if (leader) mbar_arrive_expect_tx(fb_local, STAGE_TX);
+              tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), &tmA, kb * BK, arow, U.t, fb_leader);
+              tma_load_3d_pair(smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, brow, U.t, fb_leader);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(kp.err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (leader only)
+    if (leader && lane == 0) {
+      // kind::f16, D fp32, A/B fp16 K-major, N = 256, M = 256 (the pair)
+      constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
+                                 (static_cast<uint32_t>(256 >> 4) << 24);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t use[2] = {0, 0};
+      bool ok = true;
+      for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
+        const Unit2 U = decode_unit2(u, kp);
+        for (int c = 0; c < kp.nchunks && ok; ++c) {
+          const int kb0 = chunk_begin(c, kp);
+          const int kb1 = chunk_begin(c + 1, kp);
+          for (int sl = 0; sl < U.ntile && ok; ++sl) {
+            if (!mbar_wait_cluster_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ++use[sl];
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(sl * 256);
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait_cluster_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+              const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                const bool first = (kb == kb0) && (k == 0) && (c == 0);
+                mma_f16_pair(d_tmem, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), idesc, first ? 0u : 1u);
+              }
+              mma_commit_pair(smem_u32(&empty[stage]));
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            if (ok) mma_commit_pair(smem_u32(&accf[sl]));
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(kp.err, kErrTimeout);
+      }
+      mma_commit_pair(smem_u32(drain));
+      mbar_wait_bounded(smem_u32(drain), 0, abort_flag, kWaitLimitNs);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (warps 2..5, both CTAs)
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t use[2] = {0, 0};
+    bool ok = true;
+    for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
+      const Unit2 U = decode_unit2(u, kp);
+      const int64_t il = static_cast<int64_t>(U.mp) * 256 + rank * 128 + row_in_tile;
+      const int64_t i = kp.row0 + il;
+      const float mf = kp.mf[U.t];
+      const float inv_m = kp.inv_mf[U.t];
+      for (int c = 0; c < kp.nchunks && ok; ++c) {
+        const bool last = (c == kp.nchunks - 1);
+        for (int sl = 0; sl < U.ntile; ++sl) {
+          const bool got = mbar_wait_cluster_bounded(smem_u32(&accf[sl]), use[sl] & 1, abort_flag, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          ++use[sl];
+          tc_fence_after();
+          const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
+          const int64_t j0 = static_cast<int64_t>(U.tn0 + sl) * BN;
+          if (!last) {
+#pragma unroll 1
+            for (int cb = 0; cb < BN / 32; ++cb) {
+              uint32_t v[32];
+              tmem_ld32(acc_addr + cb * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float d = __uint_as_float(v[k]);
+                const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
+                v[k] = __float_as_uint(fmaf(-mf, q, d));
+              }
+              tmem_st32(acc_addr + cb * 32, v);
+            }
+            tmem_wait_st();
+          } else {
+            uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
+#pragma unroll 1
+            for (int cb = 0; cb < BN / 32; ++cb) {
+              uint32_t v[32];
+              tmem_ld32(acc_addr + cb * 32, v);
+              tmem_wait_ld();
+              if (il < kp.p) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const int64_t j = j0 + cb * 32 + k;
+                  const float d = __uint_as_float(v[k]);
+                  const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
+                  float rr = fmaf(-mf, q, d);
+                  rr = (rr < 0.0f) ? rr + mf : rr;
+                  if (j < kp.r) Rt[j * kp.p_total + i] = static_cast<uint8_t>(__float2uint_rn(rr));
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&acce[sl]), 0));
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      atomicOr(kp.err, kErrTimeout);
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();  // the leader's MMAs are done with both CTAs' shared and tensor memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -558,11 +909,44 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   return cudaGetLastError();
 }
 
+cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  const int64_t p_total = g.p_total ? g.p_total : g.p;
+  if (!make_plane_map(&ta, g.Aplanes, g.qp, p_total, g.s, 128)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&tb, g.Bplanes, g.qp, g.r, g.s, 128)) return cudaErrorInvalidValue;
+  KParams kp{};
+  kp.p = g.p;
+  kp.r = g.r;
+  kp.row0 = g.row0;
+  kp.p_total = p_total;
+  kp.s = g.s;
+  kp.nkb = static_cast<int>(g.qp / BK);
+  kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
+  kp.tiles_m = static_cast<int>((g.p + 255) / 256);  // 256-row pair tiles
+  kp.tiles_n = static_cast<int>((g.r + sm2::BN - 1) / sm2::BN);
+  kp.pairs_n = (kp.tiles_n + 1) / 2;
+  kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
+  kp.R = g.R;
+  kp.err = g.err;
+  for (int t = 0; t < kSMax; ++t) {
+    kp.mf[t] = mc.mf[t];
+    kp.inv_mf[t] = mc.inv_mf[t];
+  }
+  cudaError_t e = cudaFuncSetAttribute(oz2_gemm2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::SMEM);
+  if (e != cudaSuccess) return e;
+  int64_t clusters = std::min<int64_t>(kp.units, g.num_sms / 2);
+  if (clusters < 1) clusters = 1;
+  oz2_gemm2sm_kernel<<<static_cast<unsigned>(2 * clusters), NUM_THREADS, sm2::SMEM, st>>>(ta, tb, kp);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
   switch (kind) {
     case kGemmMod:
+      if (g.use_2sm) return launch_2sm(g, mc, st);
       return launch_impl<256, kGemmMod>(g, mc, st);
     case kGemmExactP:
       return launch_impl<128, kGemmExactP>(g, mc, st);

@@ -124,6 +124,7 @@ struct GemmArgs {
   const int32_t* v;       // kGemmBound: [r]
   int* err;               // device error word
   int num_sms;
+  bool use_2sm = false;   // kGemmMod only: CTA-pair kernel (tcgen05 cta_group::2)
 };
 
 cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st);
