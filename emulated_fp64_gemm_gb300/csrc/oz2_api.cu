@@ -123,11 +123,10 @@ const Tables& tables() {
         mc.inv_mf[t] = 1.0f / static_cast<float>(m);
         // CRT constants
         cc.m[t] = static_cast<int>(m);
-        cc.magic32[t] = mc.magic32[t];
         Big Mt = M;
         const uint32_t rem = big_divmod_small(Mt, m);
         (void)rem;  // M is a multiple of m
-        for (int k = 0; k < kLimbs; ++k) cc.Mt[t][k] = Mt.l[k];
+        for (int k = 0; k < kLimbs16; ++k) cc.Mt16[t][k] = (Mt.l[k / 2] >> (16 * (k % 2))) & 0xFFFFu;
         Big tmp = Mt;
         const uint32_t mt_mod = big_divmod_small(tmp, m);
         uint32_t inv = 0;
@@ -136,17 +135,19 @@ const Tables& tables() {
             inv = x;
             break;
           }
-        cc.inv[t] = inv;
+        mc.crt_inv_f[t] = static_cast<float>(inv);
+        mc.crt_c[t] = mt_mod;
       }
       for (int k = 0; k < kLimbs; ++k) cc.M[k] = M.l[k];
       Big Mh = M;
       big_divmod_small(Mh, 2);
       for (int k = 0; k < kLimbs; ++k) cc.Mhalf[k] = Mh.l[k];
-      const int nl = crt_limbs(s);
-      cc.top = nl - 1;
-      const double mtop = static_cast<double>(M.l[nl - 1]) + static_cast<double>(M.l[nl - 2]) * 0x1p-32 +
-                          static_cast<double>(M.l[nl - 3]) * 0x1p-64;
-      cc.inv_Mtop = static_cast<float>(1.0 / mtop);
+      for (int k = 0; k < kLimbs16; ++k) cc.M16[k] = (M.l[k / 2] >> (16 * (k % 2))) & 0xFFFFu;
+      const int nl16 = 2 * crt_limbs(s);
+      double mest = 0.0;
+      for (int k = (nl16 > 6 ? nl16 - 6 : 0); k < nl16; ++k)  // the limbs the kernel's estimate uses
+        mest += static_cast<double>(cc.M16[k]) * std::ldexp(1.0, 16 * (k - nl16 + 1));
+      cc.inv_Mest = static_cast<float>(1.0 / mest);
       // L = M/2 - 1
       Big L = Mh;
       for (int k = 0; k < kBigLimbs; ++k) {  // subtract 1
@@ -257,7 +258,7 @@ Layout make_layout(int64_t p, int64_t q, int64_t r, int s, int64_t qp, bool stag
   L.colkey = take(r * 8);
   L.planesA = take(static_cast<size_t>(s) * p * qp * 2);
   L.planesB = take(static_cast<size_t>(s) * r * qp * 2);
-  L.R = take(static_cast<size_t>(s) * p * r);
+  L.R = take(static_cast<size_t>(s) * p * ((r + 3) / 4) * 4);  // coefficient words, 4 columns each
   if (staging) {
     L.stageA = take(static_cast<size_t>(p) * q * 8);
     L.stageB = take(static_cast<size_t>(q) * r * 8);
@@ -461,7 +462,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   if (dbg) {
     if (dbg->alpha) OZ2_CU(cudaMemcpyAsync(dbg->alpha, alpha, p * 4, cudaMemcpyDeviceToDevice, st));
     if (dbg->beta) OZ2_CU(cudaMemcpyAsync(dbg->beta, beta, r * 4, cudaMemcpyDeviceToDevice, st));
-    if (dbg->R) OZ2_CU(cudaMemcpyAsync(dbg->R, Rw, static_cast<size_t>(s) * p * r, cudaMemcpyDeviceToDevice, st));
+    if (dbg->R) OZ2_CU(launch_w_to_r(Rw, p, r, hc->mod, dbg->R, st));
     if (dbg->Ares) OZ2_CU(launch_planes_to_int8(planesA, p, q, qp, s, dbg->Ares, st));
     if (dbg->Bres) OZ2_CU(launch_planes_to_int8(planesB, r, q, qp, s, dbg->Bres, st));
     if (dbg->P) {

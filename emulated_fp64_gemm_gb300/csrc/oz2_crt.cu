@@ -13,36 +13,38 @@
 namespace oz2 {
 namespace {
 
-// Exact CRT of one output entry from its s residues (byte lanes of rv across
-// VEC entries), accumulated in 64-bit sums of 32-bit limbs.  NL limbs hold
-// every sum_t w_t M/m_t (< s M); MAXS bounds s at compile time so the
-// channel loop unrolls and every constant is an immediate operand.
-template <int NL>
-__device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConsts& cc, int k,
+// Exact CRT of one output entry.  The GEMM epilogue stores the CRT
+// coefficients w_t = R_t (M/m_t)^-1 mod m_t, so here Y = sum_t w_t (M/m_t) is
+// accumulated carry-free: with M/m_t in 16-bit limbs every term w_t L is below
+// 2^24 and each limb sum below s 2^24 < 2^29.  NL16 limbs (2 x crt_limbs(s))
+// hold every Y < s M; MAXS bounds s at compile time so the channel loop
+// unrolls with the constants as immediate operands.
+template <int NL16>
+__device__ __forceinline__ double crt_finish(const uint32_t (&acc)[NL16], const CrtConsts& cc, int k,
                                              uint64_t* xo) {
-  uint32_t Y[NL];
-  uint64_t carry = 0;
-#pragma unroll
-  for (int l = 0; l < NL; ++l) {
-    const uint64_t t = acc[l] + carry;
-    Y[l] = static_cast<uint32_t>(t);
-    carry = t >> 32;
-  }
-  // quotient estimate from the top three limbs scaled as a float (the
-  // dropped limbs change Y/M by far less than the float rounding; an estimate
+  constexpr int NL = NL16 / 2;
+  // quotient estimate k ~ round(Y / M) from all limbs as a float (an estimate
   // one off is corrected exactly below)
-  const float yf = static_cast<float>(Y[NL - 1]) + static_cast<float>(Y[NL - 2]) * 0x1p-32f +
-                   static_cast<float>(Y[NL - 3]) * 0x1p-64f;
-  const int kq = static_cast<int>(floorf(yf * cc.inv_Mtop + 0.5f));
+  // (the top six limbs only: below them the sum changes Y / M by < 2^-60)
+  float yf = 0.0f;
+#pragma unroll
+  for (int l = (NL16 > 6 ? NL16 - 6 : 0); l < NL16; ++l)
+    yf += static_cast<float>(acc[l]) * __int_as_float((127 + 16 * (l - NL16 + 1)) << 23);
+  const int kq = static_cast<int>(floorf(yf * cc.inv_Mest + 0.5f));
+  // X = Y - k M in 16-bit limbs (signed), then carries
   uint32_t X[NL];
   {
-    int64_t c = 0;
+    int32_t c = 0;
+    uint32_t limb[NL16];
 #pragma unroll
-    for (int l = 0; l < NL; ++l) {
-      const int64_t t = static_cast<int64_t>(Y[l]) - static_cast<int64_t>(kq) * cc.M[l] + c;
-      X[l] = static_cast<uint32_t>(t);
-      c = t >> 32;
+    for (int l = 0; l < NL16; ++l) {
+      const int32_t v = static_cast<int32_t>(acc[l]) - kq * static_cast<int32_t>(cc.M16[l]) + c;
+      limb[l] = static_cast<uint32_t>(v) & 0xFFFFu;
+      c = v >> 16;  // arithmetic: floor division by 2^16
     }
+#pragma unroll
+    for (int l = 0; l < NL; ++l) X[l] = limb[2 * l] | (limb[2 * l + 1] << 16);
+    // the final carry is the sign extension: |X| < 2^(32 NL - 1), so the top bit of X[NL - 1] is the sign
   }
   // exact correction into [-M/2, M/2): compare the top 64 bits, full compare on a tie
   {
@@ -52,7 +54,6 @@ __device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConst
     if (xt > ht) fix = -1;
     else if (xt < -ht - 1) fix = 1;
     else if (xt == ht || xt == -ht - 1) {
-      // tie on the top limbs: decide with all limbs (X >= M/2 or X < -M/2)
       int64_t c = 0;
       uint32_t top = 0;
 #pragma unroll
@@ -90,7 +91,6 @@ __device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConst
     xo[1] = (static_cast<uint64_t>(ext[3]) << 32) | ext[2];
     xo[2] = (static_cast<uint64_t>(ext[5]) << 32) | ext[4];
   }
-  // magnitude
   uint32_t mag[NL];
   {
     uint64_t c = neg ? 1u : 0u;
@@ -101,8 +101,7 @@ __device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConst
       c = t >> 32;
     }
   }
-  // move the top nonzero limb to position NL-1
-  int drop = 0;  // limbs shifted in from below
+  int drop = 0;
 #pragma unroll
   for (int st = 0; st < NL - 1; ++st) {
     if (mag[NL - 1] == 0) {
@@ -151,82 +150,99 @@ __device__ __forceinline__ double crt_finish(uint64_t (&acc)[NL], const CrtConst
   return __longlong_as_double(static_cast<long long>(bits));
 }
 
-// Output rows [row0, row0 + rows); R and X have p_total rows per column.
-template <int MAXS, int NL, int VEC>
+// Output rows [row0, row0 + rows).  W holds the coefficients as
+// [s][r4][p_total][4] (four consecutive columns of one row per word); X has
+// p_total rows per column.  Thread = (row i, group of 4 columns); x walks the
+// rows, y a strided set of column groups.
+template <int MAXS, int NL16>
 __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total, int64_t r,
                                                   const __grid_constant__ CrtConsts cc,
-                                                  const uint8_t* __restrict__ R,
+                                                  const uint8_t* __restrict__ Wb,
                                                   const int32_t* __restrict__ alpha,
                                                   const int32_t* __restrict__ beta,
                                                   double* __restrict__ C, int64_t ldc,
                                                   uint64_t* __restrict__ Xout) {
-  const int64_t pv = rows / VEC;
-  const int64_t groups = pv * r;
-  const int64_t plane = p_total * r;
-  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
-       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t j = g / pv;
-    const int64_t i0 = row0 + (g - j * pv) * VEC;
-    const int64_t base = j * p_total + i0;
-    uint64_t acc[VEC][NL];
+  const int64_t il = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (il >= rows) return;
+  const int64_t i = row0 + il;
+  const int64_t r4 = (r + 3) / 4;
+  const int64_t plane = r4 * p_total;  // words per channel
+  const uint32_t* W = reinterpret_cast<const uint32_t*>(Wb);
+  const int ai = alpha[i];
+  for (int64_t jg = blockIdx.y; jg < r4; jg += gridDim.y) {
+    const int64_t base = jg * p_total + i;
+    uint32_t wv[MAXS];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v)
+    for (int t = 0; t < MAXS; ++t) wv[t] = (t < cc.s) ? __ldg(W + t * plane + base) : 0u;
+    uint32_t acc[4][NL16];
 #pragma unroll
-      for (int l = 0; l < NL; ++l) acc[v][l] = 0;
+    for (int v = 0; v < 4; ++v)
+#pragma unroll
+      for (int l = 0; l < NL16; ++l) acc[v][l] = 0;
 #pragma unroll
     for (int t = 0; t < MAXS; ++t) {
       if (t < cc.s) {
-        uint32_t rv;
-        if (VEC == 4) rv = __ldg(reinterpret_cast<const uint32_t*>(R + t * plane + base));
-        else rv = __ldg(R + t * plane + base);
-        const uint32_t m = static_cast<uint32_t>(cc.m[t]);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          const uint32_t x = ((rv >> (8 * v)) & 255u) * cc.inv[t];  // < 2^16
-          const uint32_t w = x - __umulhi(x, cc.magic32[t]) * m;   // x mod m
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t w = (wv[t] >> (8 * v)) & 255u;
 #pragma unroll
-          for (int l = 0; l < NL; ++l) acc[v][l] += static_cast<uint64_t>(w) * cc.Mt[t][l];
+          for (int l = 0; l < NL16; ++l) acc[v][l] += w * cc.Mt16[t][l];
         }
       }
     }
-    const int bj = beta[j];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      const int64_t i = i0 + v;
-      C[j * ldc + i] = crt_finish<NL>(acc[v], cc, alpha[i] + bj, Xout ? Xout + (base + v) * 3 : nullptr);
+    for (int v = 0; v < 4; ++v) {
+      const int64_t j = jg * 4 + v;
+      if (j < r)
+        C[j * ldc + i] = crt_finish<NL16>(acc[v], cc, ai + beta[j], Xout ? Xout + (j * p_total + i) * 3 : nullptr);
     }
+  }
+}
+
+// Checking path: R_t[j][i] = w_t (M/m_t) mod m_t from the coefficient layout.
+__global__ void w_to_r_kernel(const uint8_t* __restrict__ W, int64_t p, int64_t r, ModConsts mc,
+                              uint8_t* __restrict__ R) {
+  const int64_t per_plane = p * r;
+  const int64_t r4 = (r + 3) / 4;
+  const int64_t n = per_plane * mc.s;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / per_plane);
+    const int64_t rem = idx - t * per_plane;
+    const int64_t j = rem / p;
+    const int64_t i = rem - j * p;
+    const uint32_t w = W[((t * r4 + j / 4) * p + i) * 4 + (j % 4)];
+    R[idx] = static_cast<uint8_t>((w * mc.crt_c[t]) % static_cast<uint32_t>(mc.m[t]));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, int s,
-                       const CrtConsts& cc, const uint8_t* R, const int32_t* alpha,
+                       const CrtConsts& cc, const uint8_t* W, const int32_t* alpha,
                        const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bool vec = (rows % 4) == 0 && (row0 % 4) == 0 && (p_total % 4) == 0;
-  const int64_t groups = (vec ? rows / 4 : rows) * r;
-  int64_t blocks = (groups + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms) * 16;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  const unsigned b = static_cast<unsigned>(blocks);
+  const int64_t gx = (rows + 255) / 256;
+  const int64_t r4 = (r + 3) / 4;
+  // about 16 blocks per SM in total; each y index walks r4 / gy column groups
+  int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
+  if (gy > r4) gy = r4;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const dim3 b(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   const int nl = crt_limbs(s);
-#define OZ2_CRT_LAUNCH(MS, NLV, V) \
-  crt_kernel<MS, NLV, V><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, R, alpha, beta, C, ldc, X)
-  if (nl == 3) {
-    if (vec) OZ2_CRT_LAUNCH(11, 3, 4);
-    else OZ2_CRT_LAUNCH(11, 3, 1);
-  } else if (nl == 4) {
-    if (vec) OZ2_CRT_LAUNCH(15, 4, 4);
-    else OZ2_CRT_LAUNCH(15, 4, 1);
-  } else {
-    if (vec) OZ2_CRT_LAUNCH(20, 5, 4);
-    else OZ2_CRT_LAUNCH(20, 5, 1);
-  }
-#undef OZ2_CRT_LAUNCH
+  if (nl == 3) crt_kernel<11, 6><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 4) crt_kernel<15, 8><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
+  else crt_kernel<20, 10><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_w_to_r(const uint8_t* W, int64_t p, int64_t r, const ModConsts& mc, uint8_t* R,
+                          cudaStream_t st) {
+  w_to_r_kernel<<<1024, 256, 0, st>>>(W, p, r, mc, R);
   count_launches(1);
   return cudaGetLastError();
 }

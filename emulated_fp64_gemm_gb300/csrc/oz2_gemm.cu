@@ -59,6 +59,7 @@ struct KParams {
   int64_t p, r;     // output rows of this launch, output columns
   int64_t row0;     // first output row (and row of A's planes) of this launch
   int64_t p_total;  // rows of R / P (their column stride)
+  int64_t r4;       // ceil(r / 4): column groups of the coefficient layout
   int s;
   int nkb;          // K blocks (qp / 64)
   int nchunks;      // ceil(nkb / KC_BLOCKS)
@@ -73,6 +74,7 @@ struct KParams {
   int* err;
   float mf[kSMax];
   float inv_mf[kSMax];
+  float wmul[kSMax];  // (M/m_t)^-1 mod m_t: the mod epilogue stores w_t = R_t wmul mod m_t
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -175,6 +177,29 @@ __device__ __forceinline__ uint64_t dyadic_key(uint32_t w, int x) {
 // equal size (+-1), each at most KC_BLOCKS long.
 __device__ __forceinline__ int chunk_begin(int c, const KParams& kp) {
   return static_cast<int>((static_cast<int64_t>(c) * kp.nkb) / kp.nchunks);
+}
+
+// Final epilogue of one 32-column block: from 32 fp32 accumulators D (exact
+// integers, |D| < 2^24) to the CRT coefficients w = (D (M/m)^-1) mod m as
+// bytes, packed four consecutive columns per 32-bit word.  FMA-pipe only:
+// rr = D - m rint(D/m) (|rr| <= 129), x = rr wm (|x| < 2^15), w = x - m rint(x/m)
+// moved into [0, m); the byte is the low byte of fp32(w + 2^23).
+__device__ __forceinline__ void final_w_words(const uint32_t (&v)[32], float mf, float inv_m, float wm,
+                                              uint32_t (&out)[8]) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t b[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float d = __uint_as_float(v[4 * g + h]);
+      const float rr = fmaf(-mf, fmaf(d, inv_m, 12582912.0f) - 12582912.0f, d);
+      const float x = rr * wm;
+      float w = fmaf(-mf, fmaf(x, inv_m, 12582912.0f) - 12582912.0f, x);
+      w = (w < 0.0f) ? w + mf : w;
+      b[h] = __float_as_uint(w + 8388608.0f);  // low byte = w
+    }
+    out[g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  }
 }
 
 // --------------------------------------------------------------------- unit decode
@@ -360,6 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t i = kp.row0 + il;                                       // global row
       const float mf = kp.mf[U.t];
       const float inv_m = kp.inv_mf[U.t];
+      const float wm = kp.wmul[U.t];
       for (int c = 0; c < kp.nchunks && ok; ++c) {
         const bool last = (c == kp.nchunks - 1);
         for (int sl = 0; sl < U.ntile; ++sl) {
@@ -393,22 +419,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_wait_st();
             } else {
               // final: R = D mod m in [0, m)
-              uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
+              // layout [t][r4][p_total][4]: four consecutive columns of one row per word
+              uint32_t* Wt = reinterpret_cast<uint32_t*>(kp.R) + static_cast<int64_t>(U.t) * kp.r4 * kp.p_total;
 #pragma unroll 1
               for (int cb = 0; cb < BN / 32; ++cb) {
                 uint32_t v[32];
                 tmem_ld32(acc_addr + cb * 32, v);
                 tmem_wait_ld();
                 if (il < kp.p) {
+                  uint32_t wd[8];
+                  final_w_words(v, mf, inv_m, wm, wd);
+                  const int64_t jg0 = (j0 + cb * 32) >> 2;
 #pragma unroll
-                  for (int k = 0; k < 32; ++k) {
-                    const int64_t j = j0 + cb * 32 + k;
-                    const float d = __uint_as_float(v[k]);
-                    const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
-                    float rr = fmaf(-mf, q, d);
-                    rr = (rr < 0.0f) ? rr + mf : rr;
-                    if (j < kp.r) Rt[j * kp.p_total + i] = static_cast<uint8_t>(__float2uint_rn(rr));
-                  }
+                  for (int g = 0; g < 8; ++g)
+                    if (jg0 + g < kp.r4) Wt[(jg0 + g) * kp.p_total + i] = wd[g];
                 }
               }
             }
@@ -503,19 +527,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // MMA with tcgen05.mma.cta_group::2: each CTA holds 128 rows of A and 128 of
 // the 256 rows of B^T in its own shared memory, and 128 rows x 256 columns of
 // the fp32 accumulator in its own tensor memory.  Per SM this needs 32 KB of
-// operands per 64-deep K stage instead of 48 KB, so six stages fit and the
-// pipeline covers 1.5x the load latency, and L2 reads drop by a third.
+// operands per 64-deep K stage instead of 48 KB, so seven stages fit and the
+// pipeline covers 1.75x the load latency, and L2 reads drop by a third.
 // The leader CTA (rank 0) issues every MMA; both producers signal the
 // leader's "full" barriers, the MMA commits are multicast to both CTAs, and
 // both epilogues signal the leader's "empty accumulator" barriers.  The chunk
 // schedule and the in-place reduction are those of the single-SM kernel.
 namespace sm2 {
-constexpr int STAGES = 6;
+constexpr int STAGES = 7;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB: this CTA's 128 rows of A
 constexpr int B_BYTES = 128 * BK * 2;      // 16 KB: this CTA's 128 of the 256 rows of B^T
 constexpr int STAGE_TX = 2 * (A_BYTES + B_BYTES);  // bytes landing per stage across the pair
-constexpr int GUARD = 16384;               // slack after the last B stage
-constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + GUARD + 256;
+constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;  // 230,656 bytes
 constexpr int BN = 256;                    // output columns per tile
 }  // namespace sm2
 
@@ -627,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES) + GUARD);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES));
   uint64_t* full = bars;                  // [STAGES] used in the leader only
   uint64_t* empty = bars + STAGES;        // [STAGES] in both CTAs
   uint64_t* accf = bars + 2 * STAGES;     // [2] in both CTAs
@@ -772,6 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int64_t i = kp.row0 + il;
       const float mf = kp.mf[U.t];
       const float inv_m = kp.inv_mf[U.t];
+      const float wm = kp.wmul[U.t];
       for (int c = 0; c < kp.nchunks && ok; ++c) {
         const bool last = (c == kp.nchunks - 1);
         for (int sl = 0; sl < U.ntile; ++sl) {
@@ -800,22 +824,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
             tmem_wait_st();
           } else {
-            uint8_t* Rt = kp.R + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
+            // layout [t][r4][p_total][4]: four consecutive columns of one row per word
+            uint32_t* Wt = reinterpret_cast<uint32_t*>(kp.R) + static_cast<int64_t>(U.t) * kp.r4 * kp.p_total;
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
               uint32_t v[32];
               tmem_ld32(acc_addr + cb * 32, v);
               tmem_wait_ld();
               if (il < kp.p) {
+                uint32_t wd[8];
+                final_w_words(v, mf, inv_m, wm, wd);
+                const int64_t jg0 = (j0 + cb * 32) >> 2;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                  const int64_t j = j0 + cb * 32 + k;
-                  const float d = __uint_as_float(v[k]);
-                  const float q = fmaf(d, inv_m, 12582912.0f) - 12582912.0f;
-                  float rr = fmaf(-mf, q, d);
-                  rr = (rr < 0.0f) ? rr + mf : rr;
-                  if (j < kp.r) Rt[j * kp.p_total + i] = static_cast<uint8_t>(__float2uint_rn(rr));
-                }
+                for (int g = 0; g < 8; ++g)
+                  if (jg0 + g < kp.r4) Wt[(jg0 + g) * kp.p_total + i] = wd[g];
               }
             }
           }
@@ -882,6 +904,7 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   kp.r = g.r;
   kp.row0 = g.row0;
   kp.p_total = p_total;
+  kp.r4 = (g.r + 3) / 4;
   kp.s = g.s;
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
@@ -899,6 +922,7 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   for (int t = 0; t < kSMax; ++t) {
     kp.mf[t] = mc.mf[t];
     kp.inv_mf[t] = mc.inv_mf[t];
+    kp.wmul[t] = mc.crt_inv_f[t];
   }
   auto kern = oz2_gemm_kernel<BN, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -919,6 +943,7 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   kp.r = g.r;
   kp.row0 = g.row0;
   kp.p_total = p_total;
+  kp.r4 = (g.r + 3) / 4;
   kp.s = g.s;
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
@@ -931,6 +956,7 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   for (int t = 0; t < kSMax; ++t) {
     kp.mf[t] = mc.mf[t];
     kp.inv_mf[t] = mc.inv_mf[t];
+    kp.wmul[t] = mc.crt_inv_f[t];
   }
   cudaError_t e = cudaFuncSetAttribute(oz2_gemm2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::SMEM);
   if (e != cudaSuccess) return e;

@@ -36,18 +36,20 @@ struct ModConsts {  // per-modulus constants, indexed by channel t
   uint32_t KH[kSMax];             // K_m + floor(m/2), K_m = m ceil(2^30/m)
   float mf[kSMax];                // m as float
   float inv_mf[kSMax];            // fl(1/m)
+  float crt_inv_f[kSMax];         // (M/m)^-1 mod m as float: the GEMM stores w = R (M/m)^-1 mod m
+  uint32_t crt_c[kSMax];          // (M/m) mod m: R = w (M/m) mod m
 };
+
+constexpr int kLimbs16 = 2 * kLimbs;  // 16-bit limbs of the same 160 bits
 
 struct CrtConsts {  // per-s CRT constants
   int s;
   int m[kSMax];
-  uint32_t inv[kSMax];            // (M/m_t)^-1 mod m_t
-  uint32_t magic32[kSMax];        // ceil(2^32/m)
-  uint32_t Mt[kSMax][kLimbs];     // M/m_t, little-endian 32-bit limbs
-  uint32_t M[kLimbs];             // M
+  uint32_t Mt16[kSMax][kLimbs16]; // M/m_t in 16-bit limbs (one u32 each)
+  uint32_t M16[kLimbs16];         // M in 16-bit limbs
+  uint32_t M[kLimbs];             // M, 32-bit limbs
   uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
-  int top;                        // NL - 1: the top limb of the CRT kernel's sums
-  float inv_Mtop;                 // 1 / (M[NL-1] + M[NL-2] 2^-32 + M[NL-3] 2^-64)
+  float inv_Mest;                 // 1 / sum_l M16[l] 2^(16(l - NL16 + 1)) over the top six limbs, NL16 = 2 crt_limbs(s)
 };
 
 // 32-bit limbs the CRT kernel uses for sum_t w_t M/m_t < s M: enough for
@@ -116,7 +118,8 @@ struct GemmArgs {
   int s;                  // number of channels (planes)
   const uint16_t* Aplanes;  // [s][p][qp]
   const uint16_t* Bplanes;  // [s][r][qp]
-  uint8_t* R;             // kGemmMod: [s][r][p]
+  uint8_t* R;             // kGemmMod: CRT coefficients w_t = R_t (M/m_t)^-1 mod m_t,
+                          // [s][ceil(r/4)][p_total][4] (4 consecutive columns of a row per word)
   int32_t* P;             // kGemmExactP: [s][r][p]
   uint64_t* rowkey;       // kGemmBound: [p]
   uint64_t* colkey;       // kGemmBound: [r]
@@ -134,7 +137,9 @@ cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, i
                        const CrtConsts& cc, const uint8_t* R, const int32_t* alpha,
                        const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st);
 
-// debug copies
+// debug copies: R_t = w_t (M/m_t) mod m_t from the stored CRT coefficients w_t
+cudaError_t launch_w_to_r(const uint8_t* W, int64_t p, int64_t r, const ModConsts& mc, uint8_t* R,
+                          cudaStream_t st);
 cudaError_t launch_planes_to_int8(const uint16_t* planes, int64_t rows, int64_t q, int64_t qp,
                                   int s, int8_t* out, cudaStream_t st);
 

@@ -63,6 +63,26 @@ __device__ __forceinline__ uint64_t ceil_shift(uint64_t mant, int sh) {
   return q + ((mant & ((1ull << d) - 1)) != 0 ? 1 : 0);
 }
 
+// ceil(|x| 2^k) for a double x (bits b) whose scaled value is below 2^21,
+// with 32-bit operations: |x| = m 2^E, m < 2^53; the top 32 bits of m and a
+// sticky bit for the rest suffice because the result needs at most 21 bits.
+__device__ __forceinline__ uint32_t ceil_scaled_small(uint64_t b, int k) {
+  const uint32_t hi = static_cast<uint32_t>(b >> 32);
+  const int eb = static_cast<int>((hi >> 20) & 0x7FF);
+  const uint32_t lo = static_cast<uint32_t>(b);
+  if (eb == 0) return static_cast<uint32_t>(ceil_shift(b & ((1ull << 52) - 1), -1074 + k));  // subnormal
+  // m = 2^52 + frac; top 32 bits: m >> 21, the rest sticky
+  const uint32_t m32 = ((hi & 0xFFFFF) | 0x100000u) << 11 | (lo >> 21);
+  const bool st = (lo & 0x1FFFFF) != 0;
+  // value = m32 2^(E + 21 + k), E = eb - 1075
+  const int sh = eb - 1075 + 21 + k;  // <= 0 for results below 2^21
+  const int d = -sh;
+  if (d >= 32) return 1u;             // nonzero and below 1
+  const uint32_t q = m32 >> d;
+  const bool rem = st || (d > 0 && (m32 & ((1u << d) - 1u)) != 0);
+  return q + (rem ? 1u : 0u);
+}
+
 // max { h : S * 2^h <= L } for S > 0, with L given by (Lbits, Lnorm).
 __device__ __forceinline__ int max_shift_le_L(uint64_t S, const BoundConsts& bc) {
   const int sb = 64 - __clzll(static_cast<long long>(S));
@@ -118,9 +138,8 @@ __global__ void sumsq_rows_kernel(const double* __restrict__ A, int64_t p, int64
   const int64_t l1 = min(q, l0 + cols_per_block);
   uint64_t s = 0;
   for (int64_t l = l0; l < l1; ++l) {
-    const Dec d = decode(A[l * lda + i]);
-    const uint64_t c = ceil_shift(d.mant, d.E + kF - e);
-    s += c * c;
+    const uint32_t c = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(A[l * lda + i])), kF - e);
+    s += static_cast<uint64_t>(c) * c;
   }
   if (s) atomicAdd(reinterpret_cast<unsigned long long*>(sum + i), static_cast<unsigned long long>(s));
 }
@@ -136,9 +155,8 @@ __global__ void sumsq_cols_kernel(const double* __restrict__ B, int64_t q, int64
   const int64_t l1 = min(q, l0 + seg);
   uint64_t s = 0;
   for (int64_t l = l0 + lane; l < l1; l += 32) {
-    const Dec d = decode(B[j * ldb + l]);
-    const uint64_t c = ceil_shift(d.mant, d.E + kF - e);
-    s += c * c;
+    const uint32_t c = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(B[j * ldb + l])), kF - e);
+    s += static_cast<uint64_t>(c) * c;
   }
   for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0 && s) atomicAdd(reinterpret_cast<unsigned long long*>(sum + j), static_cast<unsigned long long>(s));
