@@ -190,6 +190,8 @@ struct Workspace {
   cudaEvent_t ev_res[kMaxBlocks] = {};
   cudaEvent_t ev_gemm[kMaxBlocks] = {};
   cudaEvent_t ev_done = nullptr;
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_bready = nullptr;
 };
 
 std::mutex g_mutex;
@@ -273,7 +275,7 @@ oz2_status workspace_sync_objects(Workspace& w) {
   if (w.aux) return OZ2_OK;
   if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-  bool ok = mk(&w.ev_ready) && mk(&w.ev_done);
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready);
   for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_gemm[b]);
   return ok ? OZ2_OK : OZ2_ERR_CUDA;
 }
@@ -356,8 +358,36 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   uint8_t* Rw = at(L.R);
   ScaleArgs sa{p, q, r, lda, ldb, A, B};
 
+  // Row blocks of the overlapped schedule: residues of block b+1 and the CRT
+  // of block b run on a second stream while the tensor cores work on the
+  // GEMMs of block b (the grouped-overlap idea of the profiling study, §10.2,
+  // applied to row blocks so that the CRT overlaps too).
+  int64_t block_rows = (p + 3) / 4;
+  block_rows = (block_rows + 255) / 256 * 256;  // whole 256-row pair tiles
+  if (block_rows < 1024) block_rows = 1024;
+  const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
+  const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;
+  if (overlap) {
+    e = workspace_sync_objects(*wsp);
+    if (e != OZ2_OK) return e;
+  }
+  const int max_bits = (hc->bound.Lbits + 1) / 2;
+  bool b_side_done = false;  // B's exponents and residue planes already enqueued (on aux)
+
   if (ev) OZ2_CU(cudaEventRecord(ev[0], st));
-  if (mode == OZ2_FAST) {
+  if (mode == OZ2_FAST && overlap) {
+    // A side on `stream`, B side (statistics, exponents, residue planes) on the second stream
+    OZ2_CU(cudaEventRecord(wsp->ev_start, st));
+    OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
+    OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
+                                      wsp->aux));
+    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
+    OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
+    OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    b_side_done = true;
+    if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
+  } else if (mode == OZ2_FAST) {
     OZ2_CU(launch_fast_exponents(sa, hc->bound, amaxA, amaxB, reinterpret_cast<uint64_t*>(at(L.sumA)),
                                  reinterpret_cast<uint64_t*>(at(L.sumB)), alpha, beta, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
@@ -392,8 +422,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(launch_accu_exponents(p, r, hc->bound, rowkey, colkey, u, v, alpha, beta, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
   }
-  // |trunc(2^alpha a)| <= sqrt(L) in fast mode; accu entries beyond the limbs take the general path
-  const int max_bits = (hc->bound.Lbits + 1) / 2;
+  // (max_bits: |trunc(2^alpha a)| <= sqrt(L) in fast mode; accu entries beyond the limbs take the general path)
   GemmArgs g{};
   g.r = r;
   g.qp = qp;
@@ -406,15 +435,6 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   g.num_sms = ds->num_sms;
   // CTA-pair GEMM (tcgen05 cta_group::2) unless OZ2_GEMM_1SM selects the single-SM kernel
   g.use_2sm = std::getenv("OZ2_GEMM_1SM") == nullptr;
-  // Row blocks of the overlapped schedule: residues of block b+1 and the CRT
-  // of block b run on a second stream while the tensor cores work on the
-  // GEMMs of block b (the grouped-overlap idea of the profiling study, §10.2,
-  // applied to row blocks so that the CRT overlaps too).
-  int64_t block_rows = (p + 3) / 4;
-  block_rows = (block_rows + 255) / 256 * 256;  // whole 256-row pair tiles
-  if (block_rows < 1024) block_rows = 1024;
-  const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
-  const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;
   if (!overlap) {
     OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
     OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
@@ -426,13 +446,13 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(launch_crt(0, p, p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
   } else {
-    e = workspace_sync_objects(*wsp);
-    if (e != OZ2_OK) return e;
     cudaStream_t aux = wsp->aux;
     auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
-    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+    if (!b_side_done)
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
                                 planesA, st));
+    if (b_side_done) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
     OZ2_CU(cudaEventRecord(wsp->ev_ready, st));
     OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
     for (int b = 1; b < nb; ++b) {

@@ -87,6 +87,12 @@ cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uin
                                   uint64_t* amaxB, uint64_t* sumA, uint64_t* sumB, int32_t* alpha,
                                   int32_t* beta, cudaStream_t st);
 
+// the same, one side at a time (rows of A / columns of B), for two streams
+cudaError_t launch_fast_exponents_rows(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
+                                       uint64_t* sumA, int32_t* alpha, cudaStream_t st);
+cudaError_t launch_fast_exponents_cols(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxB,
+                                       uint64_t* sumB, int32_t* beta, cudaStream_t st);
+
 // accu mode, first half: amax, quantised bound planes Abar [p][qp], Bbar [r][qp] (fp16),
 // and the quantisation exponents u[p], v[r].
 cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,

@@ -531,28 +531,42 @@ int device_sms() {
 }  // namespace
 
 // ----------------------------------------------------------------- launchers
-cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
-                                  uint64_t* amaxB, uint64_t* sumA, uint64_t* sumB, int32_t* alpha,
-                                  int32_t* beta, cudaStream_t st) {
+cudaError_t launch_fast_exponents_rows(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
+                                       uint64_t* sumA, int32_t* alpha, cudaStream_t st) {
   const int sms = device_sms();
   cudaMemsetAsync(amaxA, 0, a.p * sizeof(uint64_t), st);
-  cudaMemsetAsync(amaxB, 0, a.r * sizeof(uint64_t), st);
   cudaMemsetAsync(sumA, 0, a.p * sizeof(uint64_t), st);
-  cudaMemsetAsync(sumB, 0, a.r * sizeof(uint64_t), st);
   const int64_t rb = (a.p + 255) / 256;
   const int splitA = cols_split(a.q, rb, sms);
   const int64_t cpbA = (a.q + splitA - 1) / splitA;
+  amax_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA);
+  sumsq_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA, sumA);
+  fast_exp_kernel<<<static_cast<unsigned>((a.p + 255) / 256), 256, 0, st>>>(amaxA, sumA, a.p, bc, alpha);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fast_exponents_cols(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxB,
+                                       uint64_t* sumB, int32_t* beta, cudaStream_t st) {
+  const int sms = device_sms();
+  cudaMemsetAsync(amaxB, 0, a.r * sizeof(uint64_t), st);
+  cudaMemsetAsync(sumB, 0, a.r * sizeof(uint64_t), st);
   const int64_t cb = (a.r + 7) / 8;
   const int splitB = cols_split(a.q, cb, sms);
   const int64_t segB = (a.q + splitB - 1) / splitB;
-  amax_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA);
   amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
-  sumsq_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA, sumA);
   sumsq_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB, sumB);
-  fast_exp_kernel<<<static_cast<unsigned>((a.p + 255) / 256), 256, 0, st>>>(amaxA, sumA, a.p, bc, alpha);
   fast_exp_kernel<<<static_cast<unsigned>((a.r + 255) / 256), 256, 0, st>>>(amaxB, sumB, a.r, bc, beta);
-  count_launches(6);
+  count_launches(3);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uint64_t* amaxA,
+                                  uint64_t* amaxB, uint64_t* sumA, uint64_t* sumB, int32_t* alpha,
+                                  int32_t* beta, cudaStream_t st) {
+  cudaError_t e = launch_fast_exponents_rows(a, bc, amaxA, sumA, alpha, st);
+  if (e != cudaSuccess) return e;
+  return launch_fast_exponents_cols(a, bc, amaxB, sumB, beta, st);
 }
 
 cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,
