@@ -305,7 +305,8 @@ def run_ours(args, rank, world, local):
     gemm_flops = 2.0 * w.s * w.p * w.q * w.r
     achieved = gemm_flops / (stages["gemm_mod"] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roofline = {"bound": "tensor", "kernel": "oz2_gemm_kernel<256, mod>", "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": "oz2_gemm2sm_kernel (CTA-pair tcgen05, mod epilogue)",
+                "unit_of_work": "the GEMM stage of one call (all row-block launches)", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": gemm_traffic_per_launch(),
                 "peak_source": f"{how} bf16 dense burst (f16 kind::f16 runs at the bf16 rate)",
@@ -319,6 +320,8 @@ def run_ours(args, rank, world, local):
         "hbm_peak_GBps": hbm,
     }
     extra = {"impl": "ours", "roofline": roofline, "stages_ms": stages,
+             "stages_note": ("overlapped schedule: residues = residue time before the first GEMM, "
+                             "gemm_mod = span of the GEMM launches, crt = CRT time after the last GEMM"),
              "stage_bandwidth": stage_roofline, "gpu_launches": launches}
     if clk is not None:
         extra["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
