@@ -332,10 +332,13 @@ struct Outputs {  // optional checking outputs
   } while (0)
 
 // The pipeline.  ev (optional, 6 events) is recorded at the stage boundaries.
+// hostC (optional, with ldc_host): copy each finished row block of C to host
+// memory as soon as its CRT is done (the host-memory entry point).
 oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
                         const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
                         cudaStream_t st, const Outputs* dbg, cudaEvent_t* ev, uint8_t** ws_out,
-                        Layout* lay_out, bool pipelined) {
+                        Layout* lay_out, bool pipelined, double* hostC = nullptr,
+                        int64_t ldc_host = 0) {
   DeviceState* ds = nullptr;
   oz2_status e = device_state(&ds);
   if (e != OZ2_OK) return e;
@@ -444,6 +447,8 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
     OZ2_CU(launch_crt(0, p, p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
+    if (hostC)
+      OZ2_CU(cudaMemcpy2DAsync(hostC, ldc_host * 8, C, ldc * 8, p * 8, r, cudaMemcpyDeviceToHost, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
   } else {
     cudaStream_t aux = wsp->aux;
@@ -473,6 +478,9 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     for (int b = 0; b < nb; ++b) {
       OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_gemm[b], 0));
       OZ2_CU(launch_crt(b * block_rows, rows_of(b), p, r, s, hc->crt, Rw, alpha, beta, C, ldc, nullptr, aux));
+      if (hostC)
+        OZ2_CU(cudaMemcpy2DAsync(hostC + b * block_rows, ldc_host * 8, C + b * block_rows, ldc * 8,
+                                 rows_of(b) * 8, r, cudaMemcpyDeviceToHost, aux));
     }
     OZ2_CU(cudaEventRecord(wsp->ev_done, aux));
     OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_done, 0));
@@ -636,12 +644,28 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r, const double* A, i
   double* dA = reinterpret_cast<double*>(ws + L.stageA);
   double* dB = reinterpret_cast<double*>(ws + L.stageB);
   double* dC = reinterpret_cast<double*>(ws + L.stageC);
-  OZ2_CU(cudaMemcpy2DAsync(dA, p * 8, A, lda * 8, p * 8, q, cudaMemcpyHostToDevice, st));
-  OZ2_CU(cudaMemcpy2DAsync(dB, q * 8, B, ldb * 8, q * 8, r, cudaMemcpyHostToDevice, st));
-  Layout L2;
-  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2, true);
+  Workspace* wsp = nullptr;
+  uint8_t* base2 = nullptr;
+  e = get_workspace(st, L.total, &base2, &wsp);
   if (e != OZ2_OK) return e;
-  OZ2_CU(cudaMemcpy2DAsync(C, ldc * 8, dC, p * 8, p * 8, r, cudaMemcpyDeviceToHost, st));
+  e = workspace_sync_objects(*wsp);
+  if (e != OZ2_OK) return e;
+  // A on the caller's stream, B on the second stream: both copies in flight at once
+  auto upload = [](double* dst, const double* src, int64_t rows, int64_t ld, int64_t cols,
+                   cudaStream_t s2) {
+    if (ld == rows) return cudaMemcpyAsync(dst, src, rows * cols * 8, cudaMemcpyHostToDevice, s2);
+    return cudaMemcpy2DAsync(dst, rows * 8, src, ld * 8, rows * 8, cols, cudaMemcpyHostToDevice, s2);
+  };
+  OZ2_CU(cudaEventRecord(wsp->ev_start, st));
+  OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
+  OZ2_CU(upload(dB, B, q, ldb, r, wsp->aux));
+  OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
+  OZ2_CU(upload(dA, A, p, lda, q, st));
+  OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
+  Layout L2;
+  // C comes back row block by row block, each as soon as its CRT is done
+  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2, true, C, ldc);
+  if (e != OZ2_OK) return e;
   OZ2_CU(cudaStreamSynchronize(st));
   return OZ2_OK;
 }

@@ -221,3 +221,19 @@ def test_overlapped_row_blocks_match_sequential(oz2, mode):
     ref = oracle.oracle_dgemm(A, B, 14, mode)
     assert ulp_distance(C.cpu().numpy(), ref["C"]) <= ULP_TOL
     np.testing.assert_array_equal(got["R"].cpu().numpy(), np.transpose(ref["R"], (0, 2, 1)))
+
+
+def test_host_entry_point_overlapped_blocks(oz2):
+    """p = 2500: row blocks overlap, C returns block by block into a host C with ldc > p."""
+    A, B = make_matrices(2500, 200, 150, 0.5, 66)
+    hA = torch.from_numpy(np.asfortranarray(A)).pin_memory()
+    hB = torch.from_numpy(np.asfortranarray(B)).pin_memory()
+    big = torch.full((150, 2600), 3.0, dtype=torch.float64).pin_memory()  # column-major (2600 x 150), ldc 2600
+    hC = big.t()[:2500]
+    assert hC.stride() == (1, 2600)
+    oz2.dgemm_host(hA, hB, 14, "fast", out=hC)
+    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    assert ulp_distance(hC.numpy(), ref["C"]) <= ULP_TOL
+    assert np.all(big.t()[2500:].numpy() == 3.0)
+    dev = oz2.dgemm(_dev(A), _dev(B), 14, "fast").cpu().numpy()
+    np.testing.assert_array_equal(hC.numpy(), dev)
