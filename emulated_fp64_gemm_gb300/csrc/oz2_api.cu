@@ -119,6 +119,20 @@ const Tables& tables() {
           mc.w20[t][k] = static_cast<uint32_t>(w);
         }
         mc.KH[t] = static_cast<uint32_t>(m * (((1u << 30) + m - 1) / m) + m / 2);
+        {
+          // fp16 of 1024 + h: exponent 10 (bias 15 -> 25), mantissa h << 0 (h < 1024)
+          const uint32_t hbits = (25u << 10) | (m / 2);
+          mc.bias2[t] = hbits | (hbits << 16);
+        }
+        for (int wd = 0; wd < 3; ++wd) {
+          uint32_t packed = 0;
+          for (int b = 0; b < 4; ++b) {
+            uint64_t w = 1;
+            for (int e2 = 0; e2 < 8 * (4 * wd + b); ++e2) w = (w * 2) % m;
+            packed |= static_cast<uint32_t>(w) << (8 * b);
+          }
+          mc.wb[t][wd] = packed;
+        }
         mc.mf[t] = static_cast<float>(m);
         mc.inv_mf[t] = 1.0f / static_cast<float>(m);
         // CRT constants

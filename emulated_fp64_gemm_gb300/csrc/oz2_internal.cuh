@@ -34,6 +34,8 @@ struct ModConsts {  // per-modulus constants, indexed by channel t
   uint32_t w21[kSMax][3];         // 2^(21k) mod m, k = 0..2  (three 21-bit limbs)
   uint32_t w20[kSMax][4];         // 2^(20k) mod m, k = 0..3  (four 20-bit limbs)
   uint32_t KH[kSMax];             // K_m + floor(m/2), K_m = m ceil(2^30/m)
+  uint32_t wb[kSMax][3];          // byte weights 2^(8(4w+b)) mod m, packed 4 per word (dp4a)
+  uint32_t bias2[kSMax];          // fp16x2 bit pattern of (1024 + floor(m/2), 1024 + floor(m/2))
   float mf[kSMax];                // m as float
   float inv_mf[kSMax];            // fl(1/m)
   float crt_inv_f[kSMax];         // (M/m)^-1 mod m as float: the GEMM stores w = R (M/m)^-1 mod m

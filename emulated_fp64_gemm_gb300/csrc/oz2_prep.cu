@@ -286,32 +286,6 @@ __global__ void accu_exp_kernel(const uint64_t* __restrict__ key, const int32_t*
 // T mod m = (trunc(2^e x) + floor(m/2)) mod m = rho_m(trunc(2^e x)) + floor(m/2).
 // The quotient comes from one multiply-high (magic39); the value goes to fp16
 // through the bit pattern 0x6400 + v (= 1024 + v) and a packed subtraction.
-template <int NL>
-struct Limbs {
-  int32_t l[NL];
-};
-
-template <int NL>
-__device__ __forceinline__ bool split_limbs(double x, int scale, Limbs<NL>& L, uint32_t& neg,
-                                            uint64_t& mant, int& sh) {
-  constexpr int LB = (NL == 3) ? 21 : 20;
-  const Dec d = decode(x);
-  neg = d.neg;
-  mant = d.mant;
-  sh = d.E + scale;
-  if (sh > LB * NL - 53) return false;  // does not fit NL limbs: general path
-#pragma unroll
-  for (int k = 0; k < NL; ++k) {
-    const int dd = LB * k - sh;
-    uint64_t v;
-    if (dd >= 0) v = (dd < 64) ? (d.mant >> dd) : 0ull;
-    else v = d.mant << (-dd);
-    const int32_t lv = static_cast<int32_t>(v & ((1ull << LB) - 1));
-    L.l[k] = d.neg ? -lv : lv;
-  }
-  return true;
-}
-
 // General path: rho_m(+-floor(mant 2^sh)) for sh > 0 via (mant mod m)(2^sh mod m).
 __device__ int residue_general(uint64_t mant, int sh, uint32_t neg, int t, const ModConsts& mc,
                                const uint8_t* __restrict__ pow2mod) {
@@ -348,94 +322,127 @@ __device__ __forceinline__ uint32_t pack_fp16_pair(uint32_t v0, uint32_t v1, __h
 // Residues of 8 consecutive K elements of one plane row, for every modulus.
 // out points at row `row` of plane 0 (element offset l0 already applied);
 // consecutive planes are plane_stride elements apart.
-template <int NL>
+//
+// Per element: N = |trunc(2^e x)| = floor(mant 2^sh) as NW 32-bit words
+// (NW = 2 covers N < 2^64, NW = 3 N < 2^96).  The words' bytes are base-256
+// digits, so for an odd modulus m
+//   T = sum_k byte_k (2^(8k) mod m) + floor(m/2)   (two or three dp4a)
+// is below 2^20 and congruent to N + floor(m/2); one multiply-high gives
+// the exact quotient and r = T mod m = rho_m(N) + floor(m/2).  The fp16
+// value rho_m(N) comes from the bit pattern 0x6400 + r and a packed
+// subtraction; for x < 0 the result is negated by flipping the fp16 sign
+// bit, since rho_m(-N) = -rho_m(N) for odd m.  Channel 0 is m = 256 (the
+// greedy set always starts with it): rho_256 is the low byte of +-N read as
+// a signed byte.  Elements whose N does not fit NW words (accu mode only)
+// take residue_general.
+// Plain per-element path for rows that contain an element whose scaled
+// magnitude does not fit NW words (accu mode only); kept out of line so the
+// fast path's register allocation does not carry it.
+template <int NW>
+__device__ __noinline__ void residues8_general(const double* x, int scale, const ModConsts& mc,
+                                               const uint8_t* __restrict__ pow2mod,
+                                               uint16_t* __restrict__ out, int64_t plane_stride) {
+  for (int t = 0; t < mc.s; ++t) {
+    uint32_t w[4];
+    for (int e = 0; e < 8; e += 2) {
+      int v[2];
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const Dec d = decode(x[e + h2]);
+        const int sh = d.E + scale;
+        const uint32_t m = static_cast<uint32_t>(mc.m[t]);
+        const int hh = mc.half[t];
+        if (sh <= 0) {
+          const uint64_t n = (sh <= -64) ? 0ull : (d.mant >> (-sh));
+          uint32_t rm = static_cast<uint32_t>(n % m);
+          if (d.neg) rm = (rm == 0) ? 0u : m - rm;
+          v[h2] = static_cast<int>((rm + static_cast<uint32_t>(hh)) % m) - hh;
+        } else {
+          v[h2] = residue_general(d.mant, sh, d.neg, t, mc, pow2mod);
+        }
+      }
+      const __half2 hv = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
+      w[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int NW>
+__device__ __forceinline__ bool split_words(double x, int scale, uint32_t (&wd)[3], uint32_t& neg) {
+  const Dec d = decode(x);
+  neg = d.neg;
+  const int sh = d.E + scale;
+  wd[0] = wd[1] = wd[2] = 0;
+  if (sh > 32 * NW - 53) return false;
+  if (sh <= 0) {
+    const uint64_t n = (sh <= -64) ? 0ull : (d.mant >> (-sh));
+    wd[0] = static_cast<uint32_t>(n);
+    wd[1] = static_cast<uint32_t>(n >> 32);
+  } else {
+    const uint64_t lo = d.mant << sh;  // sh <= 43 < 64
+    wd[0] = static_cast<uint32_t>(lo);
+    wd[1] = static_cast<uint32_t>(lo >> 32);
+    if (NW == 3) wd[2] = static_cast<uint32_t>(d.mant >> (64 - sh));
+  }
+  return true;
+}
+
+template <int NW>
 __device__ __forceinline__ void residues8(const double (&x)[8], int scale, const ModConsts& mc,
                                           const uint8_t* __restrict__ pow2mod,
                                           uint16_t* __restrict__ out, int64_t plane_stride) {
-  Limbs<NL> L[8];
+  uint32_t wd[8][3];
   uint32_t neg[8];
-  uint64_t mant[8];
-  int sh[8];
   bool fast = true;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) fast &= split_limbs<NL>(x[e], scale, L[e], neg[e], mant[e], sh[e]);
+  for (int e = 0; e < 8; ++e) fast &= split_words<NW>(x[e], scale, wd[e], neg[e]);
   const int s = mc.s;
   if (fast) {
-    // channel 0: m = 256 (the greedy set always starts with 256), and
-    // 2^(LB k) = 0 mod 256 for k >= 1, so only the low limb matters.
+    uint32_t sgn[4];  // fp16 sign-bit mask of each element pair
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) sgn[e >> 1] = (neg[e] << 15) | (neg[e + 1] << 31);
+    // channel 0: m = 256, the low byte of +-N as a signed byte (+128 bias)
     {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const uint32_t r0 = static_cast<uint32_t>(L[e].l[0] + 128) & 255u;
-        const uint32_t r1 = static_cast<uint32_t>(L[e + 1].l[0] + 128) & 255u;
+        const uint32_t r0 = ((neg[e] ? 0u - wd[e][0] : wd[e][0]) + 128u) & 255u;
+        const uint32_t r1 = ((neg[e + 1] ? 0u - wd[e + 1][0] : wd[e + 1][0]) + 128u) & 255u;
         w[e >> 1] = pack_fp16_pair(r0, r1, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
       }
       *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     for (int t = 1; t < s; ++t) {
       const uint32_t m = static_cast<uint32_t>(mc.m[t]);
-      const uint32_t magic = mc.magic39[t];
-      const uint32_t KH = mc.KH[t];
-      uint32_t wk[NL];
-#pragma unroll
-      for (int k = 1; k < NL; ++k) wk[k] = (NL == 3) ? mc.w21[t][k] : mc.w20[t][k];
-      const __half hb = __ushort2half_rn(static_cast<unsigned short>(1024 + mc.half[t]));
-      const __half2 bias2 = __halves2half2(hb, hb);
+      const uint32_t magic = mc.magic32[t];
+      const uint32_t h = static_cast<uint32_t>(mc.half[t]);
+      const uint32_t wb0 = mc.wb[t][0], wb1 = mc.wb[t][1], wb2 = mc.wb[t][2];
+      const uint32_t b2 = mc.bias2[t];
+      const __half2 bias2 = *reinterpret_cast<const __half2*>(&b2);
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
         uint32_t rr[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t T = static_cast<uint32_t>(L[e + h].l[0]) + KH;
-#pragma unroll
-          for (int k = 1; k < NL; ++k) T += wk[k] * static_cast<uint32_t>(L[e + h].l[k]);
-          const uint32_t q = __umulhi(T, magic) >> 7;
-          rr[h] = T - q * m;  // = rho_m(x') + floor(m/2)
+        for (int k = 0; k < 2; ++k) {
+          uint32_t T = __dp4a(wd[e + k][1], wb1, __dp4a(wd[e + k][0], wb0, h));
+          if (NW == 3) T = __dp4a(wd[e + k][2], wb2, T);
+          rr[k] = T - __umulhi(T, magic) * m;  // = rho_m(N) + floor(m/2), exact for T < 2^24
         }
-        w[e >> 1] = pack_fp16_pair(rr[0], rr[1], bias2);
+        w[e >> 1] = pack_fp16_pair(rr[0], rr[1], bias2) ^ sgn[e >> 1];
       }
       *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
-    for (int t = 0; t < s; ++t) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        int v[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ee = e + h;
-          if (sh[ee] <= ((NL == 3) ? 21 : 20) * NL - 53) {
-            // this element fits the limbs; reduce it the plain way
-            const uint32_t m = static_cast<uint32_t>(mc.m[t]);
-            int64_t acc = 0;
-#pragma unroll
-            for (int k = 0; k < NL; ++k)
-              acc += static_cast<int64_t>(L[ee].l[k]) *
-                     static_cast<int64_t>(k == 0 ? 1u : ((NL == 3) ? mc.w21[t][k] : mc.w20[t][k]));
-            int64_t rm = acc % static_cast<int64_t>(m);
-            if (rm < 0) rm += m;
-            const int hh = mc.half[t];
-            v[h] = static_cast<int>((rm + hh) % m) - hh;
-          } else {
-            v[h] = residue_general(mant[ee], sh[ee], neg[ee], t, mc, pow2mod);
-          }
-        }
-        const __half2 hv = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
-        w[e >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    residues8_general<NW>(x, scale, mc, pow2mod, out, plane_stride);
   }
 }
 
 // A (column-major p x q) -> planes [s][p][qp]: each warp covers 16 rows x 16
 // K elements, so every load instruction reads two full 128-byte lines and
 // every row of every plane gets 32 contiguous bytes per warp store.
-template <int NL>
-__global__ void __launch_bounds__(256) residue_rows_kernel(const double* __restrict__ A, int64_t p,
+template <int NW>
+__global__ void __launch_bounds__(256, 3) residue_rows_kernel(const double* __restrict__ A, int64_t p,
                                                            int64_t q, int64_t lda, int64_t qp,
                                                            int64_t plane_rows,
                                                            const int32_t* __restrict__ alpha,
@@ -449,13 +456,13 @@ __global__ void __launch_bounds__(256) residue_rows_kernel(const double* __restr
   double x[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
-  residues8<NL>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, plane_rows * qp);
+  residues8<NW>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, plane_rows * qp);
 }
 
 // B (column-major q x r) -> planes [s][r][qp]: one warp per column, 8
 // consecutive K elements per lane.
-template <int NL>
-__global__ void __launch_bounds__(256) residue_cols_kernel(const double* __restrict__ B, int64_t q,
+template <int NW>
+__global__ void __launch_bounds__(256, 3) residue_cols_kernel(const double* __restrict__ B, int64_t q,
                                                            int64_t r, int64_t ldb, int64_t qp,
                                                            const int32_t* __restrict__ beta,
                                                            ModConsts mc,
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(256) residue_cols_kernel(const double* __restr
 #pragma unroll
     for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(col + k) : 0.0;
   }
-  residues8<NL>(x, beta[j], mc, pow2mod, planes + j * qp + l0, r * qp);
+  residues8<NW>(x, beta[j], mc, pow2mod, planes + j * qp + l0, r * qp);
 }
 
 __global__ void planes_to_int8_kernel(const uint16_t* __restrict__ planes, int64_t rows, int64_t q,
@@ -605,10 +612,10 @@ cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64
                                  const uint8_t* pow2mod, int max_bits, uint16_t* planes,
                                  cudaStream_t st) {
   const dim3 g(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(qp / 64));
-  if (max_bits <= 63)
-    residue_rows_kernel<3><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
+  if (max_bits <= 64)
+    residue_rows_kernel<2><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
   else
-    residue_rows_kernel<4><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
+    residue_rows_kernel<3><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -617,10 +624,10 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
                                  const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
                                  int max_bits, uint16_t* planes, cudaStream_t st) {
   const dim3 g(static_cast<unsigned>((r + 7) / 8), static_cast<unsigned>((qp + 255) / 256));
-  if (max_bits <= 63)
-    residue_cols_kernel<3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
+  if (max_bits <= 64)
+    residue_cols_kernel<2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   else
-    residue_cols_kernel<4><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
+    residue_cols_kernel<3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   count_launches(1);
   return cudaGetLastError();
 }
