@@ -679,6 +679,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // Both CTAs of the pair must be running before the collective TMEM
+  // allocation: without this cluster barrier, launches that started while
+  // other kernels occupied SMs occasionally never returned from the alloc.
+  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
