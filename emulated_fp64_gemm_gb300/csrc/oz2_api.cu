@@ -389,24 +389,43 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     if (e != OZ2_OK) return e;
   }
   const int max_bits = (hc->bound.Lbits + 1) / 2;
-  bool b_side_done = false;  // B's exponents and residue planes already enqueued (on aux)
+  bool b_side_done = false;   // B's exponents and residue planes already enqueued (on aux)
+  bool b_planes_done = false;  // B's residue planes already enqueued on `stream`
+  // fast mode: B's statistics, exponents and residue planes in one read of B
+  const bool fused_b = (mode == OZ2_FAST) && cols_fused_fast_supported(q);
+  auto rows_block = [&](int64_t r0, int64_t rows) { return ScaleArgs{rows, q, r, lda, ldb, A + r0, B}; };
 
   if (ev) OZ2_CU(cudaEventRecord(ev[0], st));
   if (mode == OZ2_FAST && overlap) {
-    // A side on `stream`, B side (statistics, exponents, residue planes) on the second stream
+    // A side on `stream` (statistics of row block 0 only: alpha_i depends on
+    // row i alone, so later blocks get theirs on the second stream), B side
+    // (statistics, exponents, residue planes) on the second stream
     OZ2_CU(cudaEventRecord(wsp->ev_start, st));
     OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
-    OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
-                                      wsp->aux));
-    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
+    if (fused_b) {
+      OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
+                                    wsp->aux));
+    } else {
+      OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
+                                        wsp->aux));
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
+    }
     OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
-    OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
+                                      reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     b_side_done = true;
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
   } else if (mode == OZ2_FAST) {
-    OZ2_CU(launch_fast_exponents(sa, hc->bound, amaxA, amaxB, reinterpret_cast<uint64_t*>(at(L.sumA)),
-                                 reinterpret_cast<uint64_t*>(at(L.sumB)), alpha, beta, st));
+    OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    if (fused_b) {
+      OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
+                                    st));
+      b_planes_done = true;
+    } else {
+      OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
+                                        st));
+    }
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
   } else {
@@ -454,7 +473,8 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   g.use_2sm = std::getenv("OZ2_GEMM_1SM") == nullptr;
   if (!overlap) {
     OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
-    OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+    if (!b_planes_done)
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
     g.p = p;
     g.row0 = 0;
@@ -476,6 +496,9 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
     for (int b = 1; b < nb; ++b) {
       const int64_t r0 = b * block_rows;
+      if (mode == OZ2_FAST)
+        OZ2_CU(launch_fast_exponents_rows(rows_block(r0, rows_of(b)), hc->bound, amaxA + r0,
+                                          reinterpret_cast<uint64_t*>(at(L.sumA)) + r0, alpha + r0, aux));
       OZ2_CU(launch_residues_rows(A + r0, rows_of(b), q, lda, qp, p, hc->mod, alpha + r0, ds->pow2mod,
                                   max_bits, planesA + r0 * qp, aux));
       OZ2_CU(cudaEventRecord(wsp->ev_res[b], aux));

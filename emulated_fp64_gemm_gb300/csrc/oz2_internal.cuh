@@ -116,6 +116,14 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
                                  const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
                                  int max_bits, uint16_t* planes, cudaStream_t st);
 
+// fast mode, B side in one read of B: beta[r] and the residue planes [s][r][qp]
+// (identical to launch_fast_exponents_cols followed by launch_residues_cols);
+// for q <= 8192 only (cols_fused_fast_supported).
+bool cols_fused_fast_supported(int64_t q);
+cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
+                                   const BoundConsts& bc, const ModConsts& mc, const uint8_t* pow2mod,
+                                   int max_bits, int32_t* beta, uint16_t* planes, cudaStream_t st);
+
 // GEMM epilogue kinds
 enum GemmKind { kGemmMod = 0, kGemmExactP = 1, kGemmBound = 2 };
 

@@ -337,11 +337,15 @@ __device__ __forceinline__ uint32_t pack_fp16_pair(uint32_t v0, uint32_t v1, __h
 // take residue_general.
 // Plain per-element path for rows that contain an element whose scaled
 // magnitude does not fit NW words (accu mode only); kept out of line so the
-// fast path's register allocation does not carry it.
-template <int NW>
-__device__ __noinline__ void residues8_general(const double* x, int scale, const ModConsts& mc,
+// fast path's register allocation does not carry it.  It reloads its eight
+// elements (src[k stride] for k < nvalid, zero beyond) from memory, so the
+// caller's register copy never needs an address.
+__device__ __noinline__ void residues8_general(const double* __restrict__ src, int64_t stride, int nvalid,
+                                               int scale, const ModConsts& mc,
                                                const uint8_t* __restrict__ pow2mod,
                                                uint16_t* __restrict__ out, int64_t plane_stride) {
+  double x[8];
+  for (int k = 0; k < 8; ++k) x[k] = (k < nvalid) ? src[k * stride] : 0.0;
   for (int t = 0; t < mc.s; ++t) {
     uint32_t w[4];
     for (int e = 0; e < 8; e += 2) {
@@ -387,8 +391,11 @@ __device__ __forceinline__ bool split_words(double x, int scale, uint32_t (&wd)[
   return true;
 }
 
+// src / stride / nvalid locate the same eight elements in memory for the
+// general path.
 template <int NW>
-__device__ __forceinline__ void residues8(const double (&x)[8], int scale, const ModConsts& mc,
+__device__ __forceinline__ void residues8(const double (&x)[8], const double* src, int64_t stride, int nvalid,
+                                          int scale, const ModConsts& mc,
                                           const uint8_t* __restrict__ pow2mod,
                                           uint16_t* __restrict__ out, int64_t plane_stride) {
   uint32_t wd[8][3];
@@ -434,7 +441,7 @@ __device__ __forceinline__ void residues8(const double (&x)[8], int scale, const
       *reinterpret_cast<uint4*>(out + t * plane_stride) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
-    residues8_general<NW>(x, scale, mc, pow2mod, out, plane_stride);
+    residues8_general(src, stride, nvalid, scale, mc, pow2mod, out, plane_stride);
   }
 }
 
@@ -456,7 +463,9 @@ __global__ void __launch_bounds__(256, 3) residue_rows_kernel(const double* __re
   double x[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
-  residues8<NW>(x, alpha[i], mc, pow2mod, planes + i * qp + l0, plane_rows * qp);
+  const int64_t nv = q - l0;
+  residues8<NW>(x, A + l0 * lda + i, lda, nv < 8 ? static_cast<int>(nv) : 8, alpha[i], mc, pow2mod,
+                planes + i * qp + l0, plane_rows * qp);
 }
 
 // B (column-major q x r) -> planes [s][r][qp]: one warp per column, 8
@@ -485,7 +494,91 @@ __global__ void __launch_bounds__(256, 3) residue_cols_kernel(const double* __re
 #pragma unroll
     for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(col + k) : 0.0;
   }
-  residues8<NW>(x, beta[j], mc, pow2mod, planes + j * qp + l0, r * qp);
+  const int64_t nv = q - l0;
+  residues8<NW>(x, col, 1, nv < 8 ? static_cast<int>(nv) : 8, beta[j], mc, pow2mod, planes + j * qp + l0,
+                r * qp);
+}
+
+// Fast mode, B side in one read of B: statistics, exponent beta_j and residue
+// planes of column j.  One block per column; thread t holds the K elements
+// [2048 c + 8 t, +8) for c < NCH in registers (q <= 2048 NCH), so the max, the
+// sum of squares and the residues all work on the same registers and B is
+// read from memory once.  Results are identical to the three-kernel path
+// (amax_cols, sumsq_cols + fast_exp, residue_cols): the reductions are exact
+// integer maxima and sums, independent of their order.
+template <int NCH, int NW>
+__global__ void __launch_bounds__(256, 2) fused_cols_fast_kernel(const double* __restrict__ B, int64_t q,
+                                                              int64_t r, int64_t ldb, int64_t qp,
+                                                              BoundConsts bc, ModConsts mc,
+                                                              const uint8_t* __restrict__ pow2mod,
+                                                              int32_t* __restrict__ beta,
+                                                              uint16_t* __restrict__ planes) {
+  __shared__ uint64_t red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t j = blockIdx.x;
+  const double* col = B + j * ldb;
+  const bool vec = (reinterpret_cast<uintptr_t>(col) & 15) == 0;
+  double x[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = c * 2048ll + tid * 8ll;
+    if (vec && l0 + 8 <= q) {
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        const double2 v = __ldg(reinterpret_cast<const double2*>(col + l0 + k));
+        x[c][k] = v.x;
+        x[c][k + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[c][k] = (l0 + k < q) ? __ldg(col + l0 + k) : 0.0;
+    }
+  }
+  // max |b| (as the bits of |b|)
+  uint64_t m = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x[c][k])) & ~(1ull << 63);
+      m = b > m ? b : m;
+    }
+  for (int o = 16; o; o >>= 1) {
+    const uint64_t y = __shfl_xor_sync(0xffffffffu, m, o);
+    m = y > m ? y : m;
+  }
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
+  __syncthreads();
+  // S = sum ceil(|b| 2^(F-e))^2
+  const int e = exp_of_bits(m);
+  uint64_t sum = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t cs = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(x[c][k])), kF - e);
+      sum += static_cast<uint64_t>(cs) * cs;
+    }
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[warp] = sum;
+  __syncthreads();
+  sum = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) sum += red[w];
+  const int bj = (sum == 0) ? 0 : (max_shift_le_L(sum, bc) >> 1) - e + kF;
+  if (tid == 0) beta[j] = bj;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = c * 2048ll + tid * 8ll;
+    if (l0 < qp) {
+      const int64_t nv = q - l0;
+      residues8<NW>(x[c], col + l0, 1, nv < 0 ? 0 : (nv < 8 ? static_cast<int>(nv) : 8), bj, mc, pow2mod,
+                    planes + j * qp + l0, r * qp);
+    }
+  }
 }
 
 __global__ void planes_to_int8_kernel(const uint16_t* __restrict__ planes, int64_t rows, int64_t q,
@@ -628,6 +721,27 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
     residue_cols_kernel<2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   else
     residue_cols_kernel<3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+bool cols_fused_fast_supported(int64_t q) { return q <= 8192; }
+
+cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
+                                   const BoundConsts& bc, const ModConsts& mc, const uint8_t* pow2mod,
+                                   int max_bits, int32_t* beta, uint16_t* planes, cudaStream_t st) {
+  if (!cols_fused_fast_supported(q) || r > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 g(static_cast<unsigned>(r));
+  const int nch = static_cast<int>((qp + 2047) / 2048);
+  if (max_bits <= 64) {
+    if (nch <= 1) fused_cols_fast_kernel<1, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    else if (nch <= 2) fused_cols_fast_kernel<2, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    else fused_cols_fast_kernel<4, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+  } else {
+    if (nch <= 1) fused_cols_fast_kernel<1, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    else if (nch <= 2) fused_cols_fast_kernel<2, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    else fused_cols_fast_kernel<4, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

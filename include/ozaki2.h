@@ -109,9 +109,11 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r,
 /*
  * ozaki2_dgemm with CUDA events recorded between its stages; synchronises
  * `stream` and writes the milliseconds of each stage to stage_ms[0..5]:
- *   0 scale statistics and exponents (fast) or bound quantisation (accu)
+ *   0 scale statistics and exponents (fast) or bound quantisation (accu);
+ *     in fast mode with q <= 8192 also B's residue planes, which one kernel
+ *     produces together with B's statistics in a single read of B
  *   1 bound GEMM and exponents (accu; 0 in fast mode)
- *   2 residue planes of A and B
+ *   2 residue planes of A and (unless made in stage 0) of B
  *   3 the s modular GEMMs with the fused mod-m_t epilogue
  *   4 CRT and inverse scaling
  *   5 the whole call
@@ -138,9 +140,11 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
  * Stage profiling.  After ozaki2_profile_begin(max_calls), each of the next
  * max_calls ozaki2_dgemm calls records CUDA events at its stage boundaries
  * without synchronising.  ozaki2_dgemm overlaps stages (row blocks: the
- * residues of block b+1 and the CRT of block b run on a second stream while
- * the GEMMs of block b run on `stream`), so here stage 2 is the residue time
- * before the first GEMM starts, stage 3 the span of all GEMM launches on
+ * statistics and residues of block b+1 and the CRT of block b run on a second
+ * stream while the GEMMs of block b run on `stream`), so here stage 0 covers
+ * the statistics of A's first row block (with all of B's side running beside
+ * it on the second stream), stage 2 is the residue time before the first GEMM
+ * starts, stage 3 the span of all GEMM launches on
  * `stream`, and stage 4 the CRT time after the last GEMM; stages 0, 1 and 5
  * are as for ozaki2_dgemm_stages, which runs the stages one after another.
  * ozaki2_profile_end synchronises those events, writes the per-stage

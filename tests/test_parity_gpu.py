@@ -84,6 +84,31 @@ def test_ragged_shapes(oz2, p, q, r, s, mode):
     _full_check(oz2, A, B, s, mode)
 
 
+@pytest.mark.parametrize("q", [2048, 3000, 8192, 8200])
+def test_fast_b_side_register_chunks_and_fallback(oz2, q):
+    # fast mode makes B's statistics and residue planes in one read of B for
+    # q <= 8192 (one, two or four 2048-element chunks per thread); q = 8200
+    # takes the separate statistics and residue kernels
+    A, B = make_matrices(40, q, 24, 0.5, q)
+    _full_check(oz2, A, B, 14, "fast")
+
+
+def test_fast_b_side_unaligned_columns(oz2):
+    # odd ldb: most columns of B start off a 16-byte boundary (scalar loads)
+    A, B = make_matrices(48, 777, 33, 2.0, 11)
+    bigB = torch.zeros((33, 781), dtype=torch.float64).t()  # (781, 33), strides (1, 781)
+    bigB[:777] = torch.from_numpy(B)
+    dB = bigB.cuda()[:777]
+    assert dB.stride() == (1, 781)
+    got = oz2.dgemm_debug(_dev(A), dB, 14, "fast", want_p=False)
+    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref["beta"])
+    np.testing.assert_array_equal(got["Bres"].cpu().numpy(), np.transpose(ref["Bres"], (0, 2, 1)))
+    assert ulp_distance(got["C"].cpu().numpy(), ref["C"]) <= ULP_TOL
+    C2 = oz2.dgemm(_dev(A), dB, 14, "fast").cpu().numpy()
+    np.testing.assert_array_equal(C2, got["C"].cpu().numpy())
+
+
 def test_leading_dimensions_larger_than_rows(oz2):
     A, B = make_matrices(150, 90, 70, 0.5, 3)
     bigA = torch.zeros((200, 90), dtype=torch.float64).t().contiguous().t()  # strides (1, 200)
