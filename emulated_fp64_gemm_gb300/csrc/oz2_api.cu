@@ -50,7 +50,7 @@ int big_bitlen(const Big& a) {
   for (int k = kBigLimbs - 1; k >= 0; --k)
     if (a.l[k]) {
       int b = 0;
-      while ((a.l[k] >> b) != 0) ++b;
+      while (b < 32 && (static_cast<uint64_t>(a.l[k]) >> b) != 0) ++b;
       return 32 * k + b;
     }
   return 0;
@@ -194,6 +194,8 @@ struct DeviceState {
 };
 
 constexpr int kMaxBlocks = 8;  // row blocks of the overlapped schedule
+constexpr int kMaxParts = 2;   // column parts of its first row block
+constexpr int kMaxTasks = kMaxBlocks + kMaxParts;  // GEMM launches
 
 struct Workspace {
   size_t bytes = 0;
@@ -202,7 +204,8 @@ struct Workspace {
   cudaStream_t aux = nullptr;
   cudaEvent_t ev_ready = nullptr;
   cudaEvent_t ev_res[kMaxBlocks] = {};
-  cudaEvent_t ev_gemm[kMaxBlocks] = {};
+  cudaEvent_t ev_gemm[kMaxTasks] = {};
+  cudaEvent_t ev_bfirst = nullptr;
   cudaEvent_t ev_done = nullptr;
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_bready = nullptr;
@@ -289,8 +292,9 @@ oz2_status workspace_sync_objects(Workspace& w) {
   if (w.aux) return OZ2_OK;
   if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready);
-  for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_gemm[b]);
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_bfirst);
+  for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]);
+  for (int t = 0; t < kMaxTasks; ++t) ok = ok && mk(&w.ev_gemm[t]);
   return ok ? OZ2_OK : OZ2_ERR_CUDA;
 }
 
@@ -394,32 +398,56 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   // fast mode: B's statistics, exponents and residue planes in one read of B
   const bool fused_b = (mode == OZ2_FAST) && cols_fused_fast_supported(q);
   auto rows_block = [&](int64_t r0, int64_t rows) { return ScaleArgs{rows, q, r, lda, ldb, A + r0, B}; };
+  // Column parts of the first row block's GEMM in the overlapped schedule: it
+  // starts once B's first part is ready, and the rest of B is made beside it.
+  // Parts are whole multiples of 512 columns (pairs of 256-column tiles); at
+  // most `want` of them.  (Splitting the last block too, so that the CRT of
+  // its first parts overlaps the GEMM of the rest, measured slower: the extra
+  // GEMM launches cost more than the hidden CRT.)
+  auto col_parts = [&](int want, int64_t* c) {
+    c[0] = 0;
+    c[1] = r;
+    if (want < 2 || r < 1024ll * want) return 1;
+    const int64_t w = (r / want + 511) / 512 * 512;
+    int n = 0;
+    for (int64_t c0 = 0; c0 < r; c0 += w) c[n++] = c0;
+    c[n] = r;
+    return n;
+  };
+  int64_t cfirst[kMaxParts + 1];
+  const int nfirst = col_parts(fused_b ? 2 : 1, cfirst);
 
   if (ev) OZ2_CU(cudaEventRecord(ev[0], st));
   if (mode == OZ2_FAST && overlap) {
     // A side on `stream` (statistics of row block 0 only: alpha_i depends on
-    // row i alone, so later blocks get theirs on the second stream), B side
-    // (statistics, exponents, residue planes) on the second stream
+    // row i alone, so later blocks get theirs on the second stream), then the
+    // B side (statistics, exponents, residue planes) on the second stream
+    // A's first-block statistics run alone first: beside B's one-read kernel
+    // (which fills every SM's registers) their blocks would hardly be scheduled
+    OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
+                                      reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     OZ2_CU(cudaEventRecord(wsp->ev_start, st));
     OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
     if (fused_b) {
-      OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
-                                    wsp->aux));
+      for (int c = 0; c < nfirst; ++c) {
+        const int64_t c0 = cfirst[c];
+        OZ2_CU(launch_cols_fused_fast(B + c0 * ldb, q, cfirst[c + 1] - c0, ldb, qp, r, hc->bound, hc->mod,
+                                      ds->pow2mod, max_bits, beta + c0, planesB + c0 * qp, wsp->aux));
+        if (c == 0) OZ2_CU(cudaEventRecord(wsp->ev_bfirst, wsp->aux));
+      }
     } else {
       OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
                                         wsp->aux));
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
     }
     OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
-    OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
-                                      reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     b_side_done = true;
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
   } else if (mode == OZ2_FAST) {
     OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     if (fused_b) {
-      OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
+      OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, r, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
                                     st));
       b_planes_done = true;
     } else {
@@ -480,7 +508,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     g.row0 = 0;
     OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
-    OZ2_CU(launch_crt(0, p, p, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
+    OZ2_CU(launch_crt(0, p, p, 0, r, r, s, hc->crt, Rw, alpha, beta, C, ldc, dbg ? dbg->X : nullptr, st));
     if (hostC)
       OZ2_CU(cudaMemcpy2DAsync(hostC, ldc_host * 8, C, ldc * 8, p * 8, r, cudaMemcpyDeviceToHost, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
@@ -491,7 +519,6 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
                                 planesA, st));
-    if (b_side_done) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
     OZ2_CU(cudaEventRecord(wsp->ev_ready, st));
     OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
     for (int b = 1; b < nb; ++b) {
@@ -503,21 +530,40 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
                                   max_bits, planesA + r0 * qp, aux));
       OZ2_CU(cudaEventRecord(wsp->ev_res[b], aux));
     }
-    if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
+    // GEMM launches on `stream`: (row block, column part)
+    struct Task {
+      int64_t row0, rows, col0, cols;
+    };
+    Task tasks[kMaxTasks];
+    int ntask = 0;
     for (int b = 0; b < nb; ++b) {
-      if (b > 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
-      g.row0 = b * block_rows;
-      g.p = rows_of(b);
-      OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
-      OZ2_CU(cudaEventRecord(wsp->ev_gemm[b], st));
+      const int np = (b == 0) ? nfirst : 1;
+      for (int c = 0; c < np; ++c) {
+        const int64_t c0 = (np == 1) ? 0 : cfirst[c];
+        const int64_t c1 = (np == 1) ? r : cfirst[c + 1];
+        if (b > 0 && c == 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
+        if (b_side_done && b == 0 && c == 0)
+          OZ2_CU(cudaStreamWaitEvent(st, (fused_b && nfirst > 1) ? wsp->ev_bfirst : wsp->ev_bready, 0));
+        if (b_side_done && b == 0 && c == 1) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
+        if (ntask == 0 && ev) OZ2_CU(cudaEventRecord(ev[3], st));
+        g.row0 = b * block_rows;
+        g.p = rows_of(b);
+        g.col0 = c0;
+        g.ncols = c1 - c0;
+        OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
+        OZ2_CU(cudaEventRecord(wsp->ev_gemm[ntask], st));
+        tasks[ntask++] = Task{g.row0, g.p, c0, c1 - c0};
+      }
     }
     if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
-    for (int b = 0; b < nb; ++b) {
-      OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_gemm[b], 0));
-      OZ2_CU(launch_crt(b * block_rows, rows_of(b), p, r, s, hc->crt, Rw, alpha, beta, C, ldc, nullptr, aux));
+    // CRT (and download) of each launch's output on the second stream
+    for (int t = 0; t < ntask; ++t) {
+      const Task& k = tasks[t];
+      OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_gemm[t], 0));
+      OZ2_CU(launch_crt(k.row0, k.rows, p, k.col0, k.cols, r, s, hc->crt, Rw, alpha, beta, C, ldc, nullptr, aux));
       if (hostC)
-        OZ2_CU(cudaMemcpy2DAsync(hostC + b * block_rows, ldc_host * 8, C + b * block_rows, ldc * 8,
-                                 rows_of(b) * 8, r, cudaMemcpyDeviceToHost, aux));
+        OZ2_CU(cudaMemcpy2DAsync(hostC + k.row0 + k.col0 * ldc_host, ldc_host * 8, C + k.row0 + k.col0 * ldc,
+                                 ldc * 8, k.rows * 8, k.cols, cudaMemcpyDeviceToHost, aux));
     }
     OZ2_CU(cudaEventRecord(wsp->ev_done, aux));
     OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_done, 0));

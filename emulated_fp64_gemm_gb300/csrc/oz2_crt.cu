@@ -8,6 +8,8 @@
 // Y = sum_t w_t (M/m_t) accumulated in 64-bit limb sums, X = Y - k M with k
 // estimated from the top limbs and corrected exactly, then the rounding is
 // done on the bits of X and the double is assembled from its fields.
+#include <algorithm>
+
 #include "oz2_internal.cuh"
 
 namespace oz2 {
@@ -19,6 +21,9 @@ namespace {
 // 2^24 and each limb sum below s 2^24 < 2^29.  NL16 limbs (2 x crt_limbs(s))
 // hold every Y < s M; MAXS bounds s at compile time so the channel loop
 // unrolls with the constants as immediate operands.
+template <int NL>
+__device__ __forceinline__ double crt_round_x(uint32_t (&X)[NL], const CrtConsts& cc, int k, uint64_t* xo);
+
 template <int NL16>
 __device__ __forceinline__ double crt_finish(const uint32_t (&acc)[NL16], const CrtConsts& cc, int k,
                                              uint64_t* xo) {
@@ -46,6 +51,13 @@ __device__ __forceinline__ double crt_finish(const uint32_t (&acc)[NL16], const 
     for (int l = 0; l < NL; ++l) X[l] = limb[2 * l] | (limb[2 * l + 1] << 16);
     // the final carry is the sign extension: |X| < 2^(32 NL - 1), so the top bit of X[NL - 1] is the sign
   }
+  return crt_round_x<NL>(X, cc, k, xo);
+}
+
+// X = Y - k M (two's complement in NL 32-bit words, within one M of the
+// target range) -> exact correction into [-M/2, M/2), then C = RN(X 2^-k).
+template <int NL>
+__device__ __forceinline__ double crt_round_x(uint32_t (&X)[NL], const CrtConsts& cc, int k, uint64_t* xo) {
   // exact correction into [-M/2, M/2): compare the top 64 bits, full compare on a tie
   {
     const int64_t xt = static_cast<int64_t>((static_cast<uint64_t>(X[NL - 1]) << 32) | X[NL - 2]);
@@ -155,7 +167,8 @@ __device__ __forceinline__ double crt_finish(const uint32_t (&acc)[NL16], const 
 // p_total rows per column.  Thread = (row i, group of 4 columns); x walks the
 // rows, y a strided set of column groups.
 template <int MAXS, int NL16>
-__global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total, int64_t r,
+__global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
+                                                  int64_t jg0, int64_t jg1, int64_t r,
                                                   const __grid_constant__ CrtConsts cc,
                                                   const uint8_t* __restrict__ Wb,
                                                   const int32_t* __restrict__ alpha,
@@ -169,7 +182,7 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, in
   const int64_t plane = r4 * p_total;  // words per channel
   const uint32_t* W = reinterpret_cast<const uint32_t*>(Wb);
   const int ai = alpha[i];
-  for (int64_t jg = blockIdx.y; jg < r4; jg += gridDim.y) {
+  for (int64_t jg = jg0 + blockIdx.y; jg < jg1; jg += gridDim.y) {
     const int64_t base = jg * p_total + i;
     uint32_t wv[MAXS];
 #pragma unroll
@@ -218,24 +231,26 @@ __global__ void w_to_r_kernel(const uint8_t* __restrict__ W, int64_t p, int64_t 
 
 }  // namespace
 
-cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, int s,
-                       const CrtConsts& cc, const uint8_t* W, const int32_t* alpha,
-                       const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st) {
+cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t col0, int64_t cols,
+                       int64_t r, int s, const CrtConsts& cc, const uint8_t* W,
+                       const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
+                       uint64_t* X, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t jg0 = col0 / 4;
+  const int64_t jg1 = std::min<int64_t>((col0 + cols + 3) / 4, (r + 3) / 4);
   const int64_t gx = (rows + 255) / 256;
-  const int64_t r4 = (r + 3) / 4;
-  // about 16 blocks per SM in total; each y index walks r4 / gy column groups
+  // about 16 blocks per SM in total; each y index walks (jg1 - jg0) / gy column groups
   int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
-  if (gy > r4) gy = r4;
+  if (gy > jg1 - jg0) gy = jg1 - jg0;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
   const dim3 b(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   const int nl = crt_limbs(s);
-  if (nl == 3) crt_kernel<11, 6><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 4) crt_kernel<15, 8><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
-  else crt_kernel<20, 10><<<b, 256, 0, st>>>(row0, rows, p_total, r, cc, W, alpha, beta, C, ldc, X);
+  if (nl == 3) crt_kernel<11, 6><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 4) crt_kernel<15, 8><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else crt_kernel<20, 10><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
   count_launches(1);
   return cudaGetLastError();
 }

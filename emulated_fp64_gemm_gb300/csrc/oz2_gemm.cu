@@ -36,6 +36,7 @@
 #include <algorithm>
 
 #include "oz2_internal.cuh"
+#include "oz2_tcgen05.cuh"
 
 namespace oz2 {
 namespace {
@@ -60,6 +61,7 @@ struct KParams {
   int64_t row0;     // first output row (and row of A's planes) of this launch
   int64_t p_total;  // rows of R / P (their column stride)
   int64_t r4;       // ceil(r / 4): column groups of the coefficient layout
+  int64_t col0;     // first output column (and row of B's planes) of this launch (CTA-pair kernel)
   int s;
   int nkb;          // K blocks (qp / 64)
   int nchunks;      // ceil(nkb / KC_BLOCKS)
@@ -87,82 +89,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused for SW128 K-major)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;             // version
-  d |= static_cast<uint64_t>(2) << 61;             // SWIZZLE_128B
-  return d;
-}
-
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major.
 template <int BN>
 __device__ __forceinline__ constexpr uint32_t instr_desc() {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
          (static_cast<uint32_t>(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-#define OZ2_REG32(v)                                                                          \
-  "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),        \
-      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), \
-      "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),           \
-      "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),           \
-      "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-#define OZ2_IREG32(v)                                                                          \
-  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),      \
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),        \
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),      \
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),      \
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-
-// 32 lanes x 32 consecutive 32-bit columns: thread = lane = tile row.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];"
-      : OZ2_REG32(v)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};" ::"r"(taddr),
-      OZ2_IREG32(v)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Order-preserving key of the dyadic value w * 2^-x (w >= 0, w < 2^31).
@@ -301,7 +232,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
               tma_load_3d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK,
                           static_cast<int>(kp.row0) + U.tm * BM, U.t, fb);
-              tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK, (U.tn0 + sl) * BN, U.t, fb);
+              tma_load_3d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK,
+                          static_cast<int>(kp.col0) + (U.tn0 + sl) * BN, U.t, fb);
               ++issued;
               if (++stage == C::STAGES) {
                 stage = 0;
@@ -399,7 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++use[sl];
           tc_fence_after();
           const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
-          const int64_t j0 = static_cast<int64_t>(U.tn0 + sl) * BN;
+          const int64_t j0 = kp.col0 + static_cast<int64_t>(U.tn0 + sl) * BN;
           if (KIND == kGemmMod) {
             if (!last) {
               // in-place reduction: D <- D - m rint(D/m), exact in fp32
@@ -710,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int kb0 = chunk_begin(c, kp);
           const int kb1 = chunk_begin(c + 1, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
-            const int brow = (U.tn0 + sl) * BN + static_cast<int>(rank) * 128;
+            const int brow = static_cast<int>(kp.col0) + (U.tn0 + sl) * BN + static_cast<int>(rank) * 128;
             for (int kb = kb0; kb < kb1; ++kb) {
               if (!mbar_wait_cluster_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
                 ok = false;
@@ -812,7 +744,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ++use[sl];
           tc_fence_after();
           const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
-          const int64_t j0 = static_cast<int64_t>(U.tn0 + sl) * BN;
+          const int64_t j0 = kp.col0 + static_cast<int64_t>(U.tn0 + sl) * BN;
           if (!last) {
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
@@ -914,7 +846,8 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
   kp.tiles_m = static_cast<int>((g.p + BM - 1) / BM);
-  kp.tiles_n = static_cast<int>((g.r + BN - 1) / BN);
+  kp.col0 = g.col0;
+  kp.tiles_n = static_cast<int>(((g.ncols ? g.ncols : g.r) + BN - 1) / BN);
   kp.pairs_n = (kp.tiles_n + 1) / 2;
   kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
   kp.R = g.R;
@@ -953,7 +886,9 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
   kp.tiles_m = static_cast<int>((g.p + 255) / 256);  // 256-row pair tiles
-  kp.tiles_n = static_cast<int>((g.r + sm2::BN - 1) / sm2::BN);
+  kp.col0 = g.col0;
+  const int64_t ncols = g.ncols ? g.ncols : g.r;
+  kp.tiles_n = static_cast<int>((ncols + sm2::BN - 1) / sm2::BN);
   kp.pairs_n = (kp.tiles_n + 1) / 2;
   kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
   kp.R = g.R;

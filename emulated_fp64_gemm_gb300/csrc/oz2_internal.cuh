@@ -116,13 +116,16 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
                                  const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
                                  int max_bits, uint16_t* planes, cudaStream_t st);
 
-// fast mode, B side in one read of B: beta[r] and the residue planes [s][r][qp]
-// (identical to launch_fast_exponents_cols followed by launch_residues_cols);
-// for q <= 8192 only (cols_fused_fast_supported).
+// fast mode, B side in one read of B: beta and the residue planes of `ncols`
+// columns (identical to launch_fast_exponents_cols followed by
+// launch_residues_cols); B, beta and planes point at the first column, plane
+// rows are plane_cols apart ([s][plane_cols][qp]).  For q <= 8192 only
+// (cols_fused_fast_supported).
 bool cols_fused_fast_supported(int64_t q);
-cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
-                                   const BoundConsts& bc, const ModConsts& mc, const uint8_t* pow2mod,
-                                   int max_bits, int32_t* beta, uint16_t* planes, cudaStream_t st);
+cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
+                                   int64_t plane_cols, const BoundConsts& bc, const ModConsts& mc,
+                                   const uint8_t* pow2mod, int max_bits, int32_t* beta, uint16_t* planes,
+                                   cudaStream_t st);
 
 // GEMM epilogue kinds
 enum GemmKind { kGemmMod = 0, kGemmExactP = 1, kGemmBound = 2 };
@@ -131,6 +134,8 @@ struct GemmArgs {
   int64_t p, r, qp;       // rows of output computed by this launch, rows of B planes, padded K
   int64_t row0 = 0;       // first row (of A's planes and of the output) of this launch
   int64_t p_total = 0;    // rows of A's planes and of R / P (0: same as p)
+  int64_t col0 = 0;       // first output column of this launch (CTA-pair kernel only)
+  int64_t ncols = 0;      // output columns of this launch (0: all r)
   int s;                  // number of channels (planes)
   const uint16_t* Aplanes;  // [s][p][qp]
   const uint16_t* Bplanes;  // [s][r][qp]
@@ -148,10 +153,12 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st);
 
-// CRT + inverse scaling of output rows [row0, row0 + rows) (R, X: p_total rows)
-cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t r, int s,
-                       const CrtConsts& cc, const uint8_t* R, const int32_t* alpha,
-                       const int32_t* beta, double* C, int64_t ldc, uint64_t* X, cudaStream_t st);
+// CRT + inverse scaling of output rows [row0, row0 + rows) and columns
+// [col0, col0 + cols) (col0 a multiple of 4; W, X: p_total rows, r columns)
+cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t col0, int64_t cols,
+                       int64_t r, int s, const CrtConsts& cc, const uint8_t* W,
+                       const int32_t* alpha, const int32_t* beta, double* C, int64_t ldc,
+                       uint64_t* X, cudaStream_t st);
 
 // debug copies: R_t = w_t (M/m_t) mod m_t from the stored CRT coefficients w_t
 cudaError_t launch_w_to_r(const uint8_t* W, int64_t p, int64_t r, const ModConsts& mc, uint8_t* R,

@@ -100,7 +100,18 @@ __global__ void amax_rows_kernel(const double* __restrict__ A, int64_t p, int64_
   const int64_t l0 = blockIdx.y * cols_per_block;
   const int64_t l1 = min(q, l0 + cols_per_block);
   uint64_t m = 0;
-  for (int64_t l = l0; l < l1; ++l) {
+  int64_t l = l0;
+  for (; l + 8 <= l1; l += 8) {  // eight loads in flight per thread
+    uint64_t b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(A + (l + k) * lda + i)));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t v = b[k] & ~(1ull << 63);
+      m = v > m ? v : m;
+    }
+  }
+  for (; l < l1; ++l) {
     const uint64_t b = static_cast<uint64_t>(__double_as_longlong(A[l * lda + i])) & ~(1ull << 63);
     m = b > m ? b : m;
   }
@@ -116,7 +127,18 @@ __global__ void amax_cols_kernel(const double* __restrict__ B, int64_t q, int64_
   const int64_t l0 = blockIdx.y * seg;
   const int64_t l1 = min(q, l0 + seg);
   uint64_t m = 0;
-  for (int64_t l = l0 + lane; l < l1; l += 32) {
+  int64_t l = l0 + lane;
+  for (; l + 7 * 32 < l1; l += 8 * 32) {  // eight loads in flight per lane
+    uint64_t b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(B + j * ldb + l + k * 32)));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t v = b[k] & ~(1ull << 63);
+      m = v > m ? v : m;
+    }
+  }
+  for (; l < l1; l += 32) {
     const uint64_t b = static_cast<uint64_t>(__double_as_longlong(B[j * ldb + l])) & ~(1ull << 63);
     m = b > m ? b : m;
   }
@@ -137,7 +159,18 @@ __global__ void sumsq_rows_kernel(const double* __restrict__ A, int64_t p, int64
   const int64_t l0 = blockIdx.y * cols_per_block;
   const int64_t l1 = min(q, l0 + cols_per_block);
   uint64_t s = 0;
-  for (int64_t l = l0; l < l1; ++l) {
+  int64_t l = l0;
+  for (; l + 8 <= l1; l += 8) {
+    uint64_t b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(A + (l + k) * lda + i)));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t c = ceil_scaled_small(b[k], kF - e);
+      s += static_cast<uint64_t>(c) * c;
+    }
+  }
+  for (; l < l1; ++l) {
     const uint32_t c = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(A[l * lda + i])), kF - e);
     s += static_cast<uint64_t>(c) * c;
   }
@@ -154,7 +187,18 @@ __global__ void sumsq_cols_kernel(const double* __restrict__ B, int64_t q, int64
   const int64_t l0 = blockIdx.y * seg;
   const int64_t l1 = min(q, l0 + seg);
   uint64_t s = 0;
-  for (int64_t l = l0 + lane; l < l1; l += 32) {
+  int64_t l = l0 + lane;
+  for (; l + 7 * 32 < l1; l += 8 * 32) {
+    uint64_t b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(B + j * ldb + l + k * 32)));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t c = ceil_scaled_small(b[k], kF - e);
+      s += static_cast<uint64_t>(c) * c;
+    }
+  }
+  for (; l < l1; l += 32) {
     const uint32_t c = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(B[j * ldb + l])), kF - e);
     s += static_cast<uint64_t>(c) * c;
   }
@@ -500,7 +544,8 @@ __global__ void __launch_bounds__(256, 3) residue_cols_kernel(const double* __re
 }
 
 // Fast mode, B side in one read of B: statistics, exponent beta_j and residue
-// planes of column j.  One block per column; thread t holds the K elements
+// planes of column j of a range of `ncols` columns (B, beta and planes point at
+// the range's first column; plane rows are plane_cols apart).  One block per column; thread t holds the K elements
 // [2048 c + 8 t, +8) for c < NCH in registers (q <= 2048 NCH), so the max, the
 // sum of squares and the residues all work on the same registers and B is
 // read from memory once.  Results are identical to the three-kernel path
@@ -508,7 +553,7 @@ __global__ void __launch_bounds__(256, 3) residue_cols_kernel(const double* __re
 // integer maxima and sums, independent of their order.
 template <int NCH, int NW>
 __global__ void __launch_bounds__(256, 2) fused_cols_fast_kernel(const double* __restrict__ B, int64_t q,
-                                                              int64_t r, int64_t ldb, int64_t qp,
+                                                              int64_t ldb, int64_t qp, int64_t plane_cols,
                                                               BoundConsts bc, ModConsts mc,
                                                               const uint8_t* __restrict__ pow2mod,
                                                               int32_t* __restrict__ beta,
@@ -576,7 +621,7 @@ __global__ void __launch_bounds__(256, 2) fused_cols_fast_kernel(const double* _
     if (l0 < qp) {
       const int64_t nv = q - l0;
       residues8<NW>(x[c], col + l0, 1, nv < 0 ? 0 : (nv < 8 ? static_cast<int>(nv) : 8), bj, mc, pow2mod,
-                    planes + j * qp + l0, r * qp);
+                    planes + j * qp + l0, plane_cols * qp);
     }
   }
 }
@@ -727,20 +772,21 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
 
 bool cols_fused_fast_supported(int64_t q) { return q <= 8192; }
 
-cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
-                                   const BoundConsts& bc, const ModConsts& mc, const uint8_t* pow2mod,
-                                   int max_bits, int32_t* beta, uint16_t* planes, cudaStream_t st) {
-  if (!cols_fused_fast_supported(q) || r > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const dim3 g(static_cast<unsigned>(r));
+cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
+                                   int64_t plane_cols, const BoundConsts& bc, const ModConsts& mc,
+                                   const uint8_t* pow2mod, int max_bits, int32_t* beta, uint16_t* planes,
+                                   cudaStream_t st) {
+  if (!cols_fused_fast_supported(q) || ncols < 1 || ncols > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 g(static_cast<unsigned>(ncols));
   const int nch = static_cast<int>((qp + 2047) / 2048);
   if (max_bits <= 64) {
-    if (nch <= 1) fused_cols_fast_kernel<1, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
-    else if (nch <= 2) fused_cols_fast_kernel<2, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
-    else fused_cols_fast_kernel<4, 2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    if (nch <= 1) fused_cols_fast_kernel<1, 2><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
+    else if (nch <= 2) fused_cols_fast_kernel<2, 2><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
+    else fused_cols_fast_kernel<4, 2><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
   } else {
-    if (nch <= 1) fused_cols_fast_kernel<1, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
-    else if (nch <= 2) fused_cols_fast_kernel<2, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
-    else fused_cols_fast_kernel<4, 3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, bc, mc, pow2mod, beta, planes);
+    if (nch <= 1) fused_cols_fast_kernel<1, 3><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
+    else if (nch <= 2) fused_cols_fast_kernel<2, 3><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
+    else fused_cols_fast_kernel<4, 3><<<g, 256, 0, st>>>(B, q, ldb, qp, plane_cols, bc, mc, pow2mod, beta, planes);
   }
   count_launches(1);
   return cudaGetLastError();

@@ -248,6 +248,27 @@ def test_overlapped_row_blocks_match_sequential(oz2, mode):
     np.testing.assert_array_equal(got["R"].cpu().numpy(), np.transpose(ref["R"], (0, 2, 1)))
 
 
+def test_overlapped_first_block_column_parts(oz2):
+    """r = 2600: the first row block's GEMM runs as two column parts (0..1535,
+    1536..2599), the first starting once B's first columns are ready."""
+    A, B = make_matrices(2500, 200, 2600, 0.5, 78)
+    dA, dB = _dev(A), _dev(B)
+    got = oz2.dgemm_debug(dA, dB, 14, "fast", want_p=False)  # stages one after another
+    C = oz2.dgemm(dA, dB, 14, "fast")                          # overlapped schedule
+    torch.cuda.synchronize()
+    Cn = C.cpu().numpy()
+    np.testing.assert_array_equal(Cn, got["C"].cpu().numpy())
+    alpha, beta = got["alpha"].cpu().numpy(), got["beta"].cpu().numpy()
+    ref_a, ref_b, _ = oracle.exponents(A, B, 14, "fast")
+    np.testing.assert_array_equal(alpha, ref_a)
+    np.testing.assert_array_equal(beta, ref_b)
+    rng = np.random.default_rng(5)
+    ii = np.concatenate([rng.integers(0, 2500, 200), [0, 1023, 1024, 2499]])
+    jj = np.concatenate([rng.integers(0, 2600, 200), [1535, 1536, 0, 2599]])
+    ref = oracle.oracle_entries(A, B, 14, "fast", ii, jj, alpha=ref_a, beta=ref_b)
+    assert ulp_distance(Cn[ii, jj], ref["C"]) <= ULP_TOL
+
+
 def test_host_entry_point_overlapped_blocks(oz2):
     """p = 2500: row blocks overlap, C returns block by block into a host C with ldc > p."""
     A, B = make_matrices(2500, 200, 150, 0.5, 66)
