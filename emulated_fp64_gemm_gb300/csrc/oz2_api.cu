@@ -162,6 +162,15 @@ const Tables& tables() {
       for (int k = (nl16 > 6 ? nl16 - 6 : 0); k < nl16; ++k)  // the limbs the kernel's estimate uses
         mest += static_cast<double>(cc.M16[k]) * std::ldexp(1.0, 16 * (k - nl16 + 1));
       cc.inv_Mest = static_cast<float>(1.0 / mest);
+      // byte limbs of M/m_t, four channels per word
+      for (int t = 0; t < s; ++t) {
+        Big Mt = M;
+        big_divmod_small(Mt, static_cast<uint32_t>(T.moduli[t]));
+        for (int b = 0; b < 2 * kLimbs16; ++b) {
+          const uint32_t byte = (Mt.l[b / 4] >> (8 * (b % 4))) & 0xFFu;
+          cc.L4[t / 4][b] |= byte << (8 * (t % 4));
+        }
+      }
       // L = M/2 - 1
       Big L = Mh;
       for (int k = 0; k < kBigLimbs; ++k) {  // subtract 1

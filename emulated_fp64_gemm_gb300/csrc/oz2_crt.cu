@@ -184,30 +184,49 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, in
   const int ai = alpha[i];
   for (int64_t jg = jg0 + blockIdx.y; jg < jg1; jg += gridDim.y) {
     const int64_t base = jg * p_total + i;
-    uint32_t wv[MAXS];
+    constexpr int NG = (MAXS + 3) / 4;  // channel groups of four
+    constexpr int NB8 = 2 * NL16;       // byte limbs
+    uint32_t wv[4 * NG];
 #pragma unroll
-    for (int t = 0; t < MAXS; ++t) wv[t] = (t < cc.s) ? __ldg(W + t * plane + base) : 0u;
-    uint32_t acc[4][NL16];
+    for (int t = 0; t < 4 * NG; ++t) wv[t] = (t < cc.s) ? __ldg(W + t * plane + base) : 0u;
+    // 4x4 byte transpose per group: word 4g + v then holds output v's channels 4g .. 4g + 3
 #pragma unroll
-    for (int v = 0; v < 4; ++v)
-#pragma unroll
-      for (int l = 0; l < NL16; ++l) acc[v][l] = 0;
-#pragma unroll
-    for (int t = 0; t < MAXS; ++t) {
-      if (t < cc.s) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint32_t w = (wv[t] >> (8 * v)) & 255u;
-#pragma unroll
-          for (int l = 0; l < NL16; ++l) acc[v][l] += w * cc.Mt16[t][l];
-        }
-      }
+    for (int g = 0; g < NG; ++g) {
+      const uint32_t lo01 = __byte_perm(wv[4 * g], wv[4 * g + 1], 0x5140u);
+      const uint32_t hi01 = __byte_perm(wv[4 * g], wv[4 * g + 1], 0x7362u);
+      const uint32_t lo23 = __byte_perm(wv[4 * g + 2], wv[4 * g + 3], 0x5140u);
+      const uint32_t hi23 = __byte_perm(wv[4 * g + 2], wv[4 * g + 3], 0x7362u);
+      wv[4 * g + 0] = __byte_perm(lo01, lo23, 0x5410u);
+      wv[4 * g + 1] = __byte_perm(lo01, lo23, 0x7632u);
+      wv[4 * g + 2] = __byte_perm(hi01, hi23, 0x5410u);
+      wv[4 * g + 3] = __byte_perm(hi01, hi23, 0x7632u);
     }
-#pragma unroll
+#pragma unroll 1
     for (int v = 0; v < 4; ++v) {
       const int64_t j = jg * 4 + v;
-      if (j < r)
-        C[j * ldc + i] = crt_finish<NL16>(acc[v], cc, ai + beta[j], Xout ? Xout + (j * p_total + i) * 3 : nullptr);
+      if (j >= r) break;
+      // Y in byte limbs: S_b = sum_t w_t byte_b(M/m_t), four channels per dp4a (S_b < 2^20)
+      uint32_t acc8[NB8];
+#pragma unroll
+      for (int b = 0; b < NB8; ++b) acc8[b] = 0;
+      // (no guards on s or on the byte count: the words past s and the table
+      // bytes past each M/m_t are zero, and a uniform branch per dp4a would
+      // cost more issue slots than the zero products)
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        uint32_t wg = wv[4 * g];
+        // (select this output's word without dynamic register indexing)
+        wg = (v == 1) ? wv[4 * g + 1] : wg;
+        wg = (v == 2) ? wv[4 * g + 2] : wg;
+        wg = (v == 3) ? wv[4 * g + 3] : wg;
+#pragma unroll
+        for (int b = 0; b < NB8; ++b) acc8[b] = __dp4a(wg, cc.L4[g][b], acc8[b]);
+      }
+      // 16-bit limb sums (each below 2^29) as the finishing step expects
+      uint32_t acc[NL16];
+#pragma unroll
+      for (int l = 0; l < NL16; ++l) acc[l] = acc8[2 * l] + (acc8[2 * l + 1] << 8);
+      C[j * ldc + i] = crt_finish<NL16>(acc, cc, ai + beta[j], Xout ? Xout + (j * p_total + i) * 3 : nullptr);
     }
   }
 }

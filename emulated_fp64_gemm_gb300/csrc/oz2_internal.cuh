@@ -52,6 +52,7 @@ struct CrtConsts {  // per-s CRT constants
   uint32_t M[kLimbs];             // M, 32-bit limbs
   uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
   float inv_Mest;                 // 1 / sum_l M16[l] 2^(16(l - NL16 + 1)) over the top six limbs, NL16 = 2 crt_limbs(s)
+  uint32_t L4[kSMax / 4][2 * kLimbs16];  // byte b of M/m_t for channels t = 4g .. 4g + 3, packed (dp4a); zero past s
 };
 
 // 32-bit limbs the CRT kernel uses for sum_t w_t M/m_t < s M: enough for
