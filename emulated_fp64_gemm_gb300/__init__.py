@@ -23,7 +23,9 @@ __all__ = [
 
 FAST = 0
 ACCU = 1
-S_MIN, S_MAX, Q_LIMIT = 2, 20, 131072
+S_MIN, S_MAX = 2, 20
+# exclusive inner-dimension limits: fast mode, accu mode, debug output P (int32)
+Q_LIMIT_FAST, Q_LIMIT_ACCU, Q_LIMIT_P = 1 << 24, 133145, 131072
 STAGE_NAMES = ["scale", "bound_gemm", "residues", "gemm_mod", "crt", "total"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

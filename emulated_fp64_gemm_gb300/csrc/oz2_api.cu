@@ -338,7 +338,7 @@ oz2_status check_args(int64_t p, int64_t q, int64_t r, const void* A, int64_t ld
   if (!A || !B || !C) return OZ2_ERR_INVALID_ARG;
   if (s < OZ2_S_MIN || s > OZ2_S_MAX) return OZ2_ERR_INVALID_ARG;
   if (mode != OZ2_FAST && mode != OZ2_ACCU) return OZ2_ERR_INVALID_ARG;
-  if (q >= OZ2_Q_LIMIT) return OZ2_ERR_Q_TOO_LARGE;
+  if (q >= (mode == OZ2_FAST ? OZ2_Q_LIMIT_FAST : OZ2_Q_LIMIT_ACCU)) return OZ2_ERR_Q_TOO_LARGE;
   if (p > (int64_t(1) << 31) - 1024 || r > (int64_t(1) << 31) - 1024) return OZ2_ERR_INVALID_ARG;
   return OZ2_OK;
 }
@@ -681,6 +681,7 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, 
                               int8_t* Bres, int32_t* P, uint8_t* R, uint64_t* X) {
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
   if (e != OZ2_OK) return e;
+  if (P && q >= OZ2_Q_LIMIT_P) return OZ2_ERR_Q_TOO_LARGE;  // |P_t| <= q 2^14 must fit int32
   std::lock_guard<std::mutex> lk(g_mutex);
   Outputs o;
   o.alpha = alpha;

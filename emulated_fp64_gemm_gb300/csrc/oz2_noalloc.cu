@@ -114,7 +114,7 @@ extern "C" oz2_status ozaki2_fast_exponents_noalloc(int64_t p, int64_t q, int64_
   if (p <= 0 || q <= 0 || r <= 0 || lda < p || ldb < q) return OZ2_ERR_INVALID_ARG;
   if (!A || !B || !alpha || !beta) return OZ2_ERR_INVALID_ARG;
   if (s < OZ2_S_MIN || s > OZ2_S_MAX) return OZ2_ERR_INVALID_ARG;
-  if (q >= OZ2_Q_LIMIT) return OZ2_ERR_Q_TOO_LARGE;
+  if (q >= OZ2_Q_LIMIT_FAST) return OZ2_ERR_Q_TOO_LARGE;
   if (p > kMaxVectors || r > kMaxVectors || p + r > kMaxVectors) return OZ2_ERR_SCRATCH_TOO_SMALL;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ2_ERR_CUDA;

@@ -16,6 +16,8 @@
 // maxima) and removes the FP64 pipe from this stage.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "oz2_internal.cuh"
 
 namespace oz2 {
@@ -502,14 +504,19 @@ __global__ void __launch_bounds__(256, 3) residue_rows_kernel(const double* __re
                                                            uint16_t* __restrict__ planes) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t i = blockIdx.x * 32ll + (warp & 1) * 16 + (lane & 15);
-  const int64_t l0 = blockIdx.y * 64ll + (warp >> 1) * 16 + (lane >> 4) * 8;
-  if (i >= p || l0 >= qp) return;
-  double x[8];
+  if (i >= p) return;
+  const int ai = alpha[i];
+  // y walks the 64-wide K blocks (more of them than the grid's y extent when q > 2^22)
+  for (int64_t kb = blockIdx.y; kb * 64 < qp; kb += gridDim.y) {
+    const int64_t l0 = kb * 64ll + (warp >> 1) * 16 + (lane >> 4) * 8;
+    if (l0 >= qp) continue;
+    double x[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
-  const int64_t nv = q - l0;
-  residues8<NW>(x, A + l0 * lda + i, lda, nv < 8 ? static_cast<int>(nv) : 8, alpha[i], mc, pow2mod,
-                planes + i * qp + l0, plane_rows * qp);
+    for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
+    const int64_t nv = q - l0;
+    residues8<NW>(x, A + l0 * lda + i, lda, nv < 8 ? static_cast<int>(nv) : 8, ai, mc, pow2mod,
+                  planes + i * qp + l0, plane_rows * qp);
+  }
 }
 
 // B (column-major q x r) -> planes [s][r][qp]: one warp per column, 8
@@ -523,24 +530,29 @@ __global__ void __launch_bounds__(256, 3) residue_cols_kernel(const double* __re
                                                            uint16_t* __restrict__ planes) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t j = blockIdx.x * 8ll + warp;
-  const int64_t l0 = blockIdx.y * 256ll + lane * 8;
-  if (j >= r || l0 >= qp) return;
-  const double* col = B + j * ldb + l0;
-  double x[8];
-  if (l0 + 8 <= q && (reinterpret_cast<uintptr_t>(col) & 15) == 0) {
+  if (j >= r) return;
+  const int bj = beta[j];
+  // y walks the 256-wide K blocks (more of them than the grid's y extent when q > 2^24 - 2^8)
+  for (int64_t kb = blockIdx.y; kb * 256 < qp; kb += gridDim.y) {
+    const int64_t l0 = kb * 256ll + lane * 8;
+    if (l0 >= qp) continue;
+    const double* col = B + j * ldb + l0;
+    double x[8];
+    if (l0 + 8 <= q && (reinterpret_cast<uintptr_t>(col) & 15) == 0) {
 #pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-      const double2 v = __ldg(reinterpret_cast<const double2*>(col + k));
-      x[k] = v.x;
-      x[k + 1] = v.y;
+      for (int k = 0; k < 8; k += 2) {
+        const double2 v = __ldg(reinterpret_cast<const double2*>(col + k));
+        x[k] = v.x;
+        x[k + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(col + k) : 0.0;
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = (l0 + k < q) ? __ldg(col + k) : 0.0;
+    const int64_t nv = q - l0;
+    residues8<NW>(x, col, 1, nv < 8 ? static_cast<int>(nv) : 8, bj, mc, pow2mod, planes + j * qp + l0,
+                  r * qp);
   }
-  const int64_t nv = q - l0;
-  residues8<NW>(x, col, 1, nv < 8 ? static_cast<int>(nv) : 8, beta[j], mc, pow2mod, planes + j * qp + l0,
-                r * qp);
 }
 
 // Fast mode, B side in one read of B: statistics, exponent beta_j and residue
@@ -749,7 +761,7 @@ cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64
                                  int64_t plane_rows, const ModConsts& mc, const int32_t* alpha,
                                  const uint8_t* pow2mod, int max_bits, uint16_t* planes,
                                  cudaStream_t st) {
-  const dim3 g(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(qp / 64));
+  const dim3 g(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(std::min<int64_t>(qp / 64, 65535)));
   if (max_bits <= 64)
     residue_rows_kernel<2><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, alpha, mc, pow2mod, planes);
   else
@@ -761,7 +773,7 @@ cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64
 cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
                                  const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
                                  int max_bits, uint16_t* planes, cudaStream_t st) {
-  const dim3 g(static_cast<unsigned>((r + 7) / 8), static_cast<unsigned>((qp + 255) / 256));
+  const dim3 g(static_cast<unsigned>((r + 7) / 8), static_cast<unsigned>(std::min<int64_t>((qp + 255) / 256, 65535)));
   if (max_bits <= 64)
     residue_cols_kernel<2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   else

@@ -34,8 +34,17 @@
  * workspace must not run concurrently from several host threads.
  *
  * Preconditions: finite inputs (an Inf/NaN entry gives an unspecified
- * result in its row of C / column of C), q < 131072 (the INT32 condition of
- * supplement §1.3, kept as the library's contract), 2 <= s <= 20.
+ * result in its row of C / column of C), 2 <= s <= 20, and the inner
+ * dimension within its mode's limit below.  The INT32 condition q < 131072
+ * of "Ozaki II supplement: INT8 range conditions and paper performance
+ * results" §1.3 bounds one unblocked accumulation; the modular GEMMs here
+ * reduce every K-block of at most 960 terms modulo m_t before the next is
+ * added (the blocking that section describes for larger q), so the result
+ * R_t = P_t mod m_t is exact for any q.  What remains: the fast-mode
+ * sum-of-squares statistic is a 64-bit sum of q terms below 2^40
+ * (q < 2^24); the accu bound product Wbar = Abar Bbar is accumulated
+ * exactly in INT32 (q 127^2 < 2^31, q <= 133144); the checking output P of
+ * ozaki2_dgemm_debug is int32 (q < 131072).
  */
 #ifndef OZAKI2_H
 #define OZAKI2_H
@@ -55,7 +64,7 @@ typedef enum {
 typedef enum {
   OZ2_OK = 0,
   OZ2_ERR_INVALID_ARG = 1,       /* bad size, leading dimension, pointer, s or mode */
-  OZ2_ERR_Q_TOO_LARGE = 2,       /* q >= 131072 */
+  OZ2_ERR_Q_TOO_LARGE = 2,       /* q at or above its mode's limit (OZ2_Q_LIMIT_*) */
   OZ2_ERR_NO_MEMORY = 3,         /* workspace allocation failed */
   OZ2_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
   OZ2_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait gave up */
@@ -66,8 +75,10 @@ typedef enum {
 /* Smallest and largest number of moduli accepted. */
 #define OZ2_S_MIN 2
 #define OZ2_S_MAX 20
-/* Exclusive upper bound on the inner dimension q. */
-#define OZ2_Q_LIMIT 131072
+/* Exclusive upper bounds on the inner dimension q (see the file comment). */
+#define OZ2_Q_LIMIT_FAST (1 << 24)   /* fast mode */
+#define OZ2_Q_LIMIT_ACCU 133145      /* accu mode: q 127^2 < 2^31 */
+#define OZ2_Q_LIMIT_P 131072         /* ozaki2_dgemm_debug with P requested: q 2^14 < 2^31 */
 
 /*
  * C = A B by Ozaki Scheme II with s moduli and the given bound mode.

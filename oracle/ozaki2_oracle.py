@@ -36,13 +36,22 @@ from fractions import Fraction
 import numpy as np
 
 # Fractional bits kept per element in the fast-mode sum-of-squares statistic
-# (reading R5).  q < 2**17 and each rounded-up term is <= 2**F, so the sum of
-# squares is < 2**57 and fits a 64-bit integer.
+# (reading R5).  Each rounded-up term is <= 2**(2F), so for q < 2**24 the sum
+# of squares is < 2**64 and fits a 64-bit integer (FAST_Q_LIMIT).
 F_FAST = 20
 # Largest magnitude of an upward-quantised bound entry: signed INT8 (reading R6).
 BOUND_QMAX = 127
-# [S] §1.3: q * 2**14 < 2**31  <=>  q < 131072.
+# [S] §1.3: q * 2**14 < 2**31  <=>  q < 131072, the bound for one unblocked
+# INT32 accumulation of a residue product.  For longer inner dimensions the
+# same section splits K into blocks, reduces each block's product modulo the
+# modulus and combines the residues; the result R_t = P_t mod m_t is the same
+# number, so the oracle computes P_t exactly (int64: |P_t| <= q 2**14) and
+# reduces it, for any q (reading R14).
 Q_LIMIT = 131072
+# Limits that remain: the 64-bit fast statistic (above) and the accu bound
+# product Wbar = Abar Bbar, an exact INT32 accumulation (q 127**2 < 2**31).
+FAST_Q_LIMIT = 1 << 24
+ACCU_Q_LIMIT = 133145
 
 
 # ----------------------------------------------------------------------------
@@ -425,8 +434,11 @@ def oracle_dgemm(A: np.ndarray, B: np.ndarray, s: int, mode: str) -> dict:
     B = np.asarray(B, dtype=np.float64)
     if A.shape[1] != B.shape[0]:
         raise ValueError("inner dimensions differ")
-    if A.shape[1] >= Q_LIMIT:
-        raise ValueError("q >= 131072 breaks the INT32 accumulation condition")
+    q = A.shape[1]
+    if mode == "fast" and q >= FAST_Q_LIMIT:
+        raise ValueError("q >= 2**24: the fast sum-of-squares statistic leaves 64 bits")
+    if mode == "accu" and q >= ACCU_Q_LIMIT:
+        raise ValueError("q * 127**2 >= 2**31: the bound product leaves INT32")
     alpha, beta, consts = exponents(A, B, s, mode)
     moduli = consts["moduli"]
     Ares = residue_planes(A, alpha, axis=1, moduli=moduli)

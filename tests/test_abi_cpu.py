@@ -56,8 +56,16 @@ def test_argument_errors_are_returned_before_any_device_work(lib):
     assert _call(lib, s=1) == 1
     assert _call(lib, s=21) == 1
     assert _call(lib, mode=2) == 1
-    assert _call(lib, q=131072, ldb=131072) == 2  # the INT32 condition q < 2^17
-    assert _call(lib, q=131071, ldb=131071) != 2
+    # inner-dimension limits per mode: the K-blocked modular GEMMs lift the
+    # single-accumulation INT32 condition q < 2^17; what remains is the 64-bit
+    # fast statistic (q < 2^24) and the INT32 accu bound product (q 127^2 < 2^31)
+    assert _call(lib, q=1 << 24, ldb=1 << 24, mode=0) == 2
+    assert _call(lib, q=(1 << 24) - 1, ldb=1 << 24, mode=0) != 2
+    assert _call(lib, q=131072, ldb=131072, mode=0) != 2
+    assert _call(lib, q=133145, ldb=133145, mode=1) == 2
+    assert _call(lib, q=133144, ldb=133144, mode=1) != 2
+    assert oz2.Q_LIMIT_ACCU == oracle.ACCU_Q_LIMIT and oz2.Q_LIMIT_FAST == oracle.FAST_Q_LIMIT
+    assert (oz2.Q_LIMIT_ACCU - 1) * 127**2 < 2**31 <= oz2.Q_LIMIT_ACCU * 127**2
 
 
 def test_no_gpu_means_a_loud_error(lib):

@@ -195,8 +195,26 @@ def test_worst_case_products_reach_the_int32_bound():
     Bres = np.full((1, q, 2), -128, dtype=np.int64)
     P = oz.products(Ares, Bres)
     assert np.all(P == q * 2**14)
+
+
+def test_inner_dimension_beyond_the_int32_condition():
+    """[S] §1.3, last paragraph: past q = 2**17 the inner dimension is blocked
+    and each block reduced modulo m_t; the residues combine to P_t mod m_t of
+    the exact product.  Pins: worst-case residues at q = 2**17 + 64 (|P_t| >
+    2**31) give R_t = (q 2**14) mod m_t; all-ones operands give C = q exactly;
+    the remaining limits are the 64-bit fast statistic and the INT32 accu bound."""
+    q = oz.Q_LIMIT + 64
+    moduli = oz.greedy_moduli(8)
+    Ares = np.full((8, 1, q), -128, dtype=np.int64)
+    Bres = np.full((8, q, 1), -128, dtype=np.int64)
+    R = oz.output_residues(oz.products(Ares, Bres), moduli)
+    assert [int(R[t, 0, 0]) for t in range(8)] == [(q * 2**14) % m for m in moduli]
+    o = oz.oracle_dgemm(np.ones((2, q)), np.ones((q, 3)), 8, "fast")
+    assert np.all(o["C"] == float(q))
+    assert (oz.FAST_Q_LIMIT - 1) * 2**(2 * oz.F_FAST) < 2**64
+    assert (oz.ACCU_Q_LIMIT - 1) * oz.BOUND_QMAX**2 < 2**31 <= oz.ACCU_Q_LIMIT * oz.BOUND_QMAX**2
     with pytest.raises(ValueError):
-        oz.oracle_dgemm(np.ones((1, oz.Q_LIMIT)), np.ones((oz.Q_LIMIT, 1)), 8, "fast")
+        oz.oracle_dgemm(np.ones((1, oz.ACCU_Q_LIMIT)), np.ones((oz.ACCU_Q_LIMIT, 1)), 8, "accu")
 
 
 def test_residue_count_closed_form():

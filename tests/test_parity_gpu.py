@@ -109,6 +109,31 @@ def test_fast_b_side_unaligned_columns(oz2):
     np.testing.assert_array_equal(C2, got["C"].cpu().numpy())
 
 
+def test_fast_inner_dimension_past_the_int32_condition(oz2):
+    """q = 140000 > 2^17: the modular GEMMs reduce every K-block modulo m_t
+    (supplement §1.3, blocked form), so every stage still matches the oracle
+    (P itself is int32 and is not requested past 2^17)."""
+    A, B = make_matrices(24, 140000, 16, 0.5, 17)
+    _full_check(oz2, A, B, 14, "fast", check_p=False)
+    with pytest.raises(oz2.Ozaki2Error):
+        oz2.dgemm_debug(_dev(A), _dev(B), 14, "fast", want_p=True)
+
+
+def test_accu_bound_product_at_its_int32_limit(oz2):
+    """q = 133144 with every quantised bound entry 127 (|a| = |b| = 127/128):
+    Wbar = q 127^2 = 2147479576, the largest INT32-exact bound product."""
+    q = oz2.Q_LIMIT_ACCU - 1
+    rng = np.random.default_rng(9)
+    A = np.where(rng.random((8, q)) < 0.5, -1.0, 1.0) * (127 / 128)
+    B = np.where(rng.random((q, 8)) < 0.5, -1.0, 1.0) * (127 / 128)
+    got = oz2.dgemm_debug(_dev(A), _dev(B), 14, "accu", want_p=False)
+    ref = oracle.oracle_dgemm(A, B, 14, "accu")
+    np.testing.assert_array_equal(got["alpha"].cpu().numpy(), ref["alpha"])
+    np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref["beta"])
+    assert ulp_distance(got["C"].cpu().numpy(), ref["C"]) <= ULP_TOL
+    assert oz2.last_error() == 0
+
+
 def test_leading_dimensions_larger_than_rows(oz2):
     A, B = make_matrices(150, 90, 70, 0.5, 3)
     bigA = torch.zeros((200, 90), dtype=torch.float64).t().contiguous().t()  # strides (1, 200)
