@@ -39,7 +39,9 @@ UNIT = "TFLOP/s"
 PAGES_BASELINE = {"n8192_s14_fast": 72.1}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "oz2_gemm_kernel_n8192_s14_fast.md")
-GEMM_SOURCE = os.path.join(ROOT, "emulated_fp64_gemm_gb300", "csrc", "oz2_gemm.cu")
+# the GEMM kernel's source files, hashed in this order against the summary's source_sha256
+GEMM_SOURCES = [os.path.join(ROOT, "emulated_fp64_gemm_gb300", "csrc", f)
+                for f in ("oz2_gemm.cu", "oz2_tcgen05.cuh")]
 CPU_SAMPLE = 512  # rows of A and columns of B in the oracle's bounded sample
 
 
@@ -66,15 +68,24 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def gemm_traffic_per_launch():
-    """DRAM bytes per GEMM launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def gemm_source_sha256():
+    h = hashlib.sha256()
+    for path in GEMM_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic_per_unit():
+    """DRAM bytes of the GEMM stage of one call (all its GEMM launches) from the
+    committed ncu summary, or None when the kernel source changed since the
+    counters were taken."""
     try:
         text = open(GEMM_PROFILE).read()
-        src = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()
+        src = gemm_source_sha256()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m = re.search(r"traffic_bytes_per_call:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h or h.group(1) != src:
         return None
@@ -306,9 +317,9 @@ def run_ours(args, rank, world, local):
     achieved = gemm_flops / (stages["gemm_mod"] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": "oz2_gemm2sm_kernel (CTA-pair tcgen05, mod epilogue)",
-                "unit_of_work": "the GEMM stage of one call (all row-block launches)", "achieved": achieved,
+                "unit_of_work": "the GEMM stage of one call (all its GEMM launches)", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": gemm_traffic_per_launch(),
+                "traffic": gemm_traffic_per_unit(),
                 "peak_source": f"{how} bf16 dense burst (f16 kind::f16 runs at the bf16 rate)",
                 "algorithmic": "2*s*p*q*r flops per launch"}
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))

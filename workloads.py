@@ -44,6 +44,9 @@ WORKLOADS = {
     "n1024_s14_fast": Workload("n1024_s14_fast", 1024, 1024, 1024, 14, "fast", 0.5, 123456),
     # a mid size whose planes (235 MB) still exceed L2: used for detailed kernel profiles
     "n2048_s14_fast": Workload("n2048_s14_fast", 2048, 2048, 2048, 14, "fast", 0.5, 123456),
+    # the headline's inner dimension at a few GB on the device: kernel profiles of the
+    # preprocessing (B's one-read kernel on 2048-column parts, A's residues at q = 8192)
+    "p2048_q8192_r4096_s14_fast": Workload("p2048_q8192_r4096_s14_fast", 2048, 8192, 4096, 14, "fast", 0.5, 123456),
     "n4096_s14_accu": Workload("n4096_s14_accu", 4096, 4096, 4096, 14, "accu", 1.0, 7),
     "n8192_s14_fast": Workload("n8192_s14_fast", 8192, 8192, 8192, 14, "fast", 0.5, 123456),
     "n8192_s14_accu": Workload("n8192_s14_accu", 8192, 8192, 8192, 14, "accu", 0.5, 123456),
