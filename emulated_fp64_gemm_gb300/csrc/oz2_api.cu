@@ -491,6 +491,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     g.v = v;
     g.err = ds->err;
     g.num_sms = ds->num_sms;
+    g.use_2sm = std::getenv("OZ2_GEMM_1SM") == nullptr;  // CTA-pair kernel, 128-column tiles
     OZ2_CU(launch_gemm(kGemmBound, g, hc->mod, st));
     OZ2_CU(launch_accu_exponents(p, r, hc->bound, rowkey, colkey, u, v, alpha, beta, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));

@@ -104,6 +104,78 @@ __device__ __forceinline__ uint64_t dyadic_key(uint32_t w, int x) {
   return (static_cast<uint64_t>(E + 4096) << 32) | static_cast<uint64_t>(w << (32 - b));
 }
 
+// Column maxima over a warp's 32 rows: each lane holds 32 keys (one per
+// column).  Five exchange steps halve the columns a lane keeps (16, 8, 4, 2,
+// 1 keys cross per step): at the step with offset o a lane keeps the upper
+// half of its remaining columns when its own bit o is set and sends the other
+// half to lane ^ o, so after the last step lane L holds the maximum of column L
+// (31 exchanges instead of 5 x 32 for one full reduction per column).
+__device__ __forceinline__ uint64_t warp_column_max(uint64_t (&kc)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const uint64_t keep = up ? kc[k + o] : kc[k];
+      const uint64_t send = up ? kc[k] : kc[k + o];
+      const uint64_t got = __shfl_xor_sync(0xffffffffu, send, o);
+      kc[k] = keep > got ? keep : got;
+    }
+  }
+  return kc[0];
+}
+
+// Epilogue of the accu bound GEMM for one BNc-column tile slot of one thread's
+// row: the chunk's fp32 sums (exact integers below 2^24) are added into the
+// int32 running sums held BNc columns further on in tensor memory.  After the
+// last chunk each entry W_ij of the row becomes the order-preserving keys of
+// W 2^-v_j (row maximum) and W 2^-u_i (column maximum over the warp's 32 rows),
+// and the maxima are taken with 64-bit atomics.
+template <int BNc>
+__device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, bool last, int64_t il, int64_t i,
+                                                     int64_t j0, int lane, const KParams& kp) {
+  const uint32_t sum_addr = acc_addr + BNc;
+  const bool row_ok = il < kp.p;
+  const int ui = (last && row_ok) ? kp.u[i] : 0;
+  uint64_t rmax = 0;
+#pragma unroll 1
+  for (int cb = 0; cb < BNc / 32; ++cb) {
+    uint32_t v[32], sacc[32];
+    tmem_ld32(acc_addr + cb * 32, v);
+    if (c > 0) tmem_ld32(sum_addr + cb * 32, sacc);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int add = __float2int_rn(__uint_as_float(v[k]));
+      sacc[k] = (c > 0) ? static_cast<uint32_t>(static_cast<int>(sacc[k]) + add) : static_cast<uint32_t>(add);
+    }
+    if (!last) {
+      tmem_st32(sum_addr + cb * 32, sacc);
+    } else {
+      // row: max_j key(W_ij 2^-v_j); column: max_i key(W_ij 2^-u_i)
+      uint64_t kc[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int64_t j = j0 + cb * 32 + k;
+        const bool valid = row_ok && (j < kp.r);
+        const uint32_t w = valid ? sacc[k] : 0u;
+        if (valid) {
+          const uint64_t kr = dyadic_key(w, kp.v[j]);
+          rmax = kr > rmax ? kr : rmax;
+        }
+        kc[k] = valid ? dyadic_key(w, ui) : 0ull;
+      }
+      const uint64_t cmax = warp_column_max(kc, lane);
+      const int64_t jl = j0 + cb * 32 + lane;
+      if (cmax && jl < kp.r)
+        atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + jl), static_cast<unsigned long long>(cmax));
+    }
+  }
+  if (last && rmax)
+    atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), static_cast<unsigned long long>(rmax));
+  if (!last) tmem_wait_st();
+}
+
 // First K block of chunk c: the nkb blocks are split into nchunks chunks of
 // equal size (+-1), each at most KC_BLOCKS long.
 __device__ __forceinline__ int chunk_begin(int c, const KParams& kp) {
@@ -368,8 +440,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
               }
             }
+          } else if (KIND == kGemmBound) {
+            bound_epilogue_chunk<BN>(acc_addr, c, last, il, i, j0, lane, kp);
           } else {
-            // drain the chunk into the int32 running sum at column offset +128
+            // exact P: drain the chunk into the int32 running sum at column offset +128
             const uint32_t sum_addr = acc_addr + 128;
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
@@ -385,7 +459,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               if (!last) {
                 tmem_st32(sum_addr + cb * 32, sacc);
-              } else if (KIND == kGemmExactP) {
+              } else {
                 int32_t* Pt = kp.P + static_cast<int64_t>(U.t) * kp.p_total * kp.r;
                 if (il < kp.p) {
 #pragma unroll
@@ -394,31 +468,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (j < kp.r) Pt[j * kp.p_total + i] = static_cast<int32_t>(sacc[k]);
                   }
                 }
-              } else {
-                // kGemmBound: row max of W 2^-v_j, column max of W 2^-u_i
-                const int ui = (il < kp.p) ? kp.u[i] : 0;
-                uint64_t rmax = 0;
-#pragma unroll 4
-                for (int k = 0; k < 32; ++k) {
-                  const int64_t j = j0 + cb * 32 + k;
-                  const bool valid = (il < kp.p) && (j < kp.r);
-                  const uint32_t w = valid ? sacc[k] : 0u;
-                  if (valid) {
-                    const uint64_t kr = dyadic_key(w, kp.v[j]);
-                    rmax = kr > rmax ? kr : rmax;
-                  }
-                  uint64_t kc = valid ? dyadic_key(w, ui) : 0ull;
-#pragma unroll
-                  for (int o = 16; o; o >>= 1) {
-                    const uint64_t x = __shfl_xor_sync(0xffffffffu, kc, o);
-                    kc = x > kc ? x : kc;
-                  }
-                  if (lane == 0 && kc && j < kp.r)
-                    atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + j),
-                              static_cast<unsigned long long>(kc));
-                }
-                if (rmax) atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i),
-                                    static_cast<unsigned long long>(rmax));
               }
             }
             if (!last) tmem_wait_st();
@@ -465,14 +514,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // leader's "full" barriers, the MMA commits are multicast to both CTAs, and
 // both epilogues signal the leader's "empty accumulator" barriers.  The chunk
 // schedule and the in-place reduction are those of the single-SM kernel.
-namespace sm2 {
-constexpr int STAGES = 7;
-constexpr int A_BYTES = BM * BK * 2;       // 16 KB: this CTA's 128 rows of A
-constexpr int B_BYTES = 128 * BK * 2;      // 16 KB: this CTA's 128 of the 256 rows of B^T
-constexpr int STAGE_TX = 2 * (A_BYTES + B_BYTES);  // bytes landing per stage across the pair
-constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;  // 230,656 bytes
-constexpr int BN = 256;                    // output columns per tile
-}  // namespace sm2
+// BN2 = 256 columns per tile for the modular GEMMs; 128 for the accu bound
+// GEMM, whose TMEM slots also hold an int32 running sum beside the
+// accumulator (columns [256 sl, +128) and [256 sl + 128, +128)).
+template <int BN2>
+struct Cfg2 {
+  static constexpr int BN = BN2;                             // output columns per tile
+  static constexpr int A_BYTES = BM * BK * 2;                // 16 KB: this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN2 / 2) * BK * 2;         // this CTA's half of the tile's rows of B^T
+  static constexpr int STAGES = (BN2 == 256) ? 7 : 9;
+  static constexpr int STAGE_TX = 2 * (A_BYTES + B_BYTES);   // bytes landing per stage across the pair
+  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;  // 230,656 / 222,464 bytes
+};
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -574,10 +627,14 @@ __device__ __forceinline__ Unit2 decode_unit2(int64_t u, const KParams& kp) {
   return U;
 }
 
+template <int BN2, int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     oz2_gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ KParams kp) {
-  using namespace sm2;
+  using C2 = Cfg2<BN2>;
+  constexpr int BN = C2::BN, A_BYTES = C2::A_BYTES, B_BYTES = C2::B_BYTES, STAGES = C2::STAGES,
+                STAGE_TX = C2::STAGE_TX;
+  static_assert(KIND == kGemmMod || KIND == kGemmBound, "CTA-pair epilogues: mod and bound");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -642,7 +699,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int kb0 = chunk_begin(c, kp);
           const int kb1 = chunk_begin(c + 1, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
-            const int brow = static_cast<int>(kp.col0) + (U.tn0 + sl) * BN + static_cast<int>(rank) * 128;
+            const int brow = static_cast<int>(kp.col0) + (U.tn0 + sl) * BN + static_cast<int>(rank) * (BN / 2);
             for (int kb = kb0; kb < kb1; ++kb) {
               if (!mbar_wait_cluster_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
                 ok = false;
@@ -669,8 +726,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (leader only)
     if (leader && lane == 0) {
-      // kind::f16, D fp32, A/B fp16 K-major, N = 256, M = 256 (the pair)
-      constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
+      // kind::f16, D fp32, A/B fp16 K-major, N = BN, M = 256 (the pair)
+      constexpr uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                  (static_cast<uint32_t>(256 >> 4) << 24);
       int stage = 0;
       uint32_t phase = 0;
@@ -699,7 +756,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {
-                const bool first = (kb == kb0) && (k == 0) && (c == 0);
+                // mod: the chunks accumulate on the reduced value; bound: each chunk starts from zero
+                const bool first = (kb == kb0) && (k == 0) && (KIND != kGemmMod || c == 0);
                 mma_f16_pair(d_tmem, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), idesc, first ? 0u : 1u);
               }
               mma_commit_pair(smem_u32(&empty[stage]));
@@ -745,7 +803,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
           const int64_t j0 = kp.col0 + static_cast<int64_t>(U.tn0 + sl) * BN;
-          if (!last) {
+          if (KIND == kGemmBound) {
+            bound_epilogue_chunk<BN>(acc_addr, c, last, il, i, j0, lane, kp);
+          } else if (!last) {
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
               uint32_t v[32];
@@ -871,11 +931,13 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   return cudaGetLastError();
 }
 
+template <int BN2, int KIND>
 cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
+  using C2 = Cfg2<BN2>;
   CUtensorMap ta, tb;
   const int64_t p_total = g.p_total ? g.p_total : g.p;
   if (!make_plane_map(&ta, g.Aplanes, g.qp, p_total, g.s, 128)) return cudaErrorInvalidValue;
-  if (!make_plane_map(&tb, g.Bplanes, g.qp, g.r, g.s, 128)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&tb, g.Bplanes, g.qp, g.r, g.s, BN2 / 2)) return cudaErrorInvalidValue;
   KParams kp{};
   kp.p = g.p;
   kp.r = g.r;
@@ -888,21 +950,26 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   kp.tiles_m = static_cast<int>((g.p + 255) / 256);  // 256-row pair tiles
   kp.col0 = g.col0;
   const int64_t ncols = g.ncols ? g.ncols : g.r;
-  kp.tiles_n = static_cast<int>((ncols + sm2::BN - 1) / sm2::BN);
+  kp.tiles_n = static_cast<int>((ncols + BN2 - 1) / BN2);
   kp.pairs_n = (kp.tiles_n + 1) / 2;
   kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
   kp.R = g.R;
+  kp.rowkey = g.rowkey;
+  kp.colkey = g.colkey;
+  kp.u = g.u;
+  kp.v = g.v;
   kp.err = g.err;
   for (int t = 0; t < kSMax; ++t) {
     kp.mf[t] = mc.mf[t];
     kp.inv_mf[t] = mc.inv_mf[t];
     kp.wmul[t] = mc.crt_inv_f[t];
   }
-  cudaError_t e = cudaFuncSetAttribute(oz2_gemm2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::SMEM);
+  auto kern = oz2_gemm2sm_kernel<BN2, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C2::SMEM);
   if (e != cudaSuccess) return e;
   int64_t clusters = std::min<int64_t>(kp.units, g.num_sms / 2);
   if (clusters < 1) clusters = 1;
-  oz2_gemm2sm_kernel<<<static_cast<unsigned>(2 * clusters), NUM_THREADS, sm2::SMEM, st>>>(ta, tb, kp);
+  kern<<<static_cast<unsigned>(2 * clusters), NUM_THREADS, C2::SMEM, st>>>(ta, tb, kp);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -912,11 +979,12 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
 cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, cudaStream_t st) {
   switch (kind) {
     case kGemmMod:
-      if (g.use_2sm) return launch_2sm(g, mc, st);
+      if (g.use_2sm) return launch_2sm<256, kGemmMod>(g, mc, st);
       return launch_impl<256, kGemmMod>(g, mc, st);
     case kGemmExactP:
       return launch_impl<128, kGemmExactP>(g, mc, st);
     case kGemmBound:
+      if (g.use_2sm) return launch_2sm<128, kGemmBound>(g, mc, st);
       return launch_impl<128, kGemmBound>(g, mc, st);
   }
   return cudaErrorInvalidValue;
