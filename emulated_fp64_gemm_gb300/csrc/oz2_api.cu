@@ -218,6 +218,11 @@ struct Workspace {
   cudaEvent_t ev_done = nullptr;
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_bready = nullptr;
+  // host entry point: uploads of A's row blocks and B's column parts on their own stream
+  cudaStream_t up = nullptr;
+  cudaEvent_t ev_io = nullptr;
+  cudaEvent_t ev_upA[kMaxBlocks] = {};
+  cudaEvent_t ev_upB[kMaxParts] = {};
 };
 
 std::mutex g_mutex;
@@ -300,9 +305,11 @@ Layout make_layout(int64_t p, int64_t q, int64_t r, int s, int64_t qp, bool stag
 oz2_status workspace_sync_objects(Workspace& w) {
   if (w.aux) return OZ2_OK;
   if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
+  if (cudaStreamCreateWithFlags(&w.up, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_bfirst);
-  for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]);
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_bfirst) && mk(&w.ev_io);
+  for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_upA[b]);
+  for (int c = 0; c < kMaxParts; ++c) ok = ok && mk(&w.ev_upB[c]);
   for (int t = 0; t < kMaxTasks; ++t) ok = ok && mk(&w.ev_gemm[t]);
   return ok ? OZ2_OK : OZ2_ERR_CUDA;
 }
@@ -358,14 +365,29 @@ struct Outputs {  // optional checking outputs
     if ((call) != cudaSuccess) return OZ2_ERR_CUDA;  \
   } while (0)
 
+// Host buffers of the host-memory entry point: A and B are uploaded into the
+// device staging copies the pipeline reads, C is downloaded from its device copy.
+struct HostIO {
+  const double* A;
+  int64_t lda;
+  const double* B;
+  int64_t ldb;
+  double* C;
+  int64_t ldc;
+};
+
 // The pipeline.  ev (optional, 6 events) is recorded at the stage boundaries.
-// hostC (optional, with ldc_host): copy each finished row block of C to host
-// memory as soon as its CRT is done (the host-memory entry point).
+// io (optional): the host-memory entry point.  A (lda = p) and B (ldb = q)
+// are then device staging buffers that the pipeline fills from io->A and
+// io->B itself, piece by piece in the order the overlapped schedule consumes
+// them, and each finished part of C is copied to io->C as soon as its CRT is
+// done.
 oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
                         const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
                         cudaStream_t st, const Outputs* dbg, cudaEvent_t* ev, uint8_t** ws_out,
-                        Layout* lay_out, bool pipelined, double* hostC = nullptr,
-                        int64_t ldc_host = 0) {
+                        Layout* lay_out, bool pipelined, const HostIO* io = nullptr) {
+  double* hostC = io ? io->C : nullptr;
+  const int64_t ldc_host = io ? io->ldc : 0;
   DeviceState* ds = nullptr;
   oz2_status e = device_state(&ds);
   if (e != OZ2_OK) return e;
@@ -425,6 +447,41 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   };
   int64_t cfirst[kMaxParts + 1];
   const int nfirst = col_parts(fused_b ? 2 : 1, cfirst);
+  auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
+
+  // Host entry point: uploads into the staging copies A, B.  In the overlapped
+  // fast schedule they go on their own stream in the order the schedule
+  // consumes them (A's row block 0, B's column parts, A's later row blocks),
+  // each followed by an event its consumers wait for; otherwise all first.
+  const bool staged = io != nullptr && mode == OZ2_FAST && overlap;
+  auto upload_rows = [&](int64_t r0, int64_t rows, cudaStream_t s2) {  // A rows [r0, r0 + rows)
+    return cudaMemcpy2DAsync(const_cast<double*>(A) + r0, lda * 8, io->A + r0, io->lda * 8, rows * 8, q,
+                             cudaMemcpyHostToDevice, s2);
+  };
+  auto upload_cols = [&](int64_t c0, int64_t cols, cudaStream_t s2) {  // B columns [c0, c0 + cols)
+    double* dst = const_cast<double*>(B) + c0 * ldb;
+    const double* src = io->B + c0 * io->ldb;
+    if (io->ldb == q && ldb == q) return cudaMemcpyAsync(dst, src, q * cols * 8, cudaMemcpyHostToDevice, s2);
+    return cudaMemcpy2DAsync(dst, ldb * 8, src, io->ldb * 8, q * 8, cols, cudaMemcpyHostToDevice, s2);
+  };
+  if (io && !staged) {
+    OZ2_CU(upload_rows(0, p, st));
+    OZ2_CU(upload_cols(0, r, st));
+  } else if (staged) {
+    cudaStream_t up = wsp->up;
+    OZ2_CU(cudaEventRecord(wsp->ev_io, st));  // after this stream's earlier work on the staging copies
+    OZ2_CU(cudaStreamWaitEvent(up, wsp->ev_io, 0));
+    OZ2_CU(upload_rows(0, rows_of(0), up));
+    OZ2_CU(cudaEventRecord(wsp->ev_upA[0], up));
+    for (int c = 0; c < nfirst; ++c) {
+      OZ2_CU(upload_cols(cfirst[c], cfirst[c + 1] - cfirst[c], up));
+      OZ2_CU(cudaEventRecord(wsp->ev_upB[c], up));
+    }
+    for (int b = 1; b < nb; ++b) {
+      OZ2_CU(upload_rows(b * block_rows, rows_of(b), up));
+      OZ2_CU(cudaEventRecord(wsp->ev_upA[b], up));
+    }
+  }
 
   if (ev) OZ2_CU(cudaEventRecord(ev[0], st));
   if (mode == OZ2_FAST && overlap) {
@@ -433,6 +490,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     // B side (statistics, exponents, residue planes) on the second stream
     // A's first-block statistics run alone first: beside B's one-read kernel
     // (which fills every SM's registers) their blocks would hardly be scheduled
+    if (staged) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_upA[0], 0));
     OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
                                       reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     OZ2_CU(cudaEventRecord(wsp->ev_start, st));
@@ -440,11 +498,13 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     if (fused_b) {
       for (int c = 0; c < nfirst; ++c) {
         const int64_t c0 = cfirst[c];
+        if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[c], 0));
         OZ2_CU(launch_cols_fused_fast(B + c0 * ldb, q, cfirst[c + 1] - c0, ldb, qp, r, hc->bound, hc->mod,
                                       ds->pow2mod, max_bits, beta + c0, planesB + c0 * qp, wsp->aux));
         if (c == 0) OZ2_CU(cudaEventRecord(wsp->ev_bfirst, wsp->aux));
       }
     } else {
+      if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[0], 0));  // one part: all of B
       OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
                                         wsp->aux));
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
@@ -524,7 +584,6 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     if (ev) OZ2_CU(cudaEventRecord(ev[5], st));
   } else {
     cudaStream_t aux = wsp->aux;
-    auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
     if (!b_side_done)
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
@@ -533,6 +592,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
     for (int b = 1; b < nb; ++b) {
       const int64_t r0 = b * block_rows;
+      if (staged) OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_upA[b], 0));
       if (mode == OZ2_FAST)
         OZ2_CU(launch_fast_exponents_rows(rows_block(r0, rows_of(b)), hc->bound, amaxA + r0,
                                           reinterpret_cast<uint64_t*>(at(L.sumA)) + r0, alpha + r0, aux));
@@ -738,27 +798,11 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r, const double* A, i
   double* dA = reinterpret_cast<double*>(ws + L.stageA);
   double* dB = reinterpret_cast<double*>(ws + L.stageB);
   double* dC = reinterpret_cast<double*>(ws + L.stageC);
-  Workspace* wsp = nullptr;
-  uint8_t* base2 = nullptr;
-  e = get_workspace(st, L.total, &base2, &wsp);
-  if (e != OZ2_OK) return e;
-  e = workspace_sync_objects(*wsp);
-  if (e != OZ2_OK) return e;
-  // A on the caller's stream, B on the second stream: both copies in flight at once
-  auto upload = [](double* dst, const double* src, int64_t rows, int64_t ld, int64_t cols,
-                   cudaStream_t s2) {
-    if (ld == rows) return cudaMemcpyAsync(dst, src, rows * cols * 8, cudaMemcpyHostToDevice, s2);
-    return cudaMemcpy2DAsync(dst, rows * 8, src, ld * 8, rows * 8, cols, cudaMemcpyHostToDevice, s2);
-  };
-  OZ2_CU(cudaEventRecord(wsp->ev_start, st));
-  OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
-  OZ2_CU(upload(dB, B, q, ldb, r, wsp->aux));
-  OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
-  OZ2_CU(upload(dA, A, p, lda, q, st));
-  OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
+  // the pipeline uploads A and B itself, piece by piece as its schedule needs
+  // them, and returns C row block by row block as each CRT finishes
+  const HostIO io{A, lda, B, ldb, C, ldc};
   Layout L2;
-  // C comes back row block by row block, each as soon as its CRT is done
-  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2, true, C, ldc);
+  e = run_pipeline(p, q, r, dA, p, dB, q, dC, p, s, mode, st, nullptr, nullptr, nullptr, &L2, true, &io);
   if (e != OZ2_OK) return e;
   OZ2_CU(cudaStreamSynchronize(st));
   return OZ2_OK;

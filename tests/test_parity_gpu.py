@@ -203,6 +203,29 @@ def test_host_entry_point(oz2):
     assert ulp_distance(C, ref["C"]) <= ULP_TOL
 
 
+def test_host_entry_point_staged_uploads(oz2):
+    """The host entry point uploads A by row blocks and B by column parts as the
+    schedule needs them: strided host operands (lda > p, ldb > q), two column
+    parts (r = 2600) and two calls in a row through the same staging copies must
+    each give the device entry point's C bit for bit."""
+    for seed in (81, 82):
+        A, B = make_matrices(2500, 300, 2600, 0.5, seed)
+        hAbig = torch.zeros((300, 2504), dtype=torch.float64)  # column-major 2504 x 300
+        hAbig.t()[:2500] = torch.from_numpy(A)
+        hBbig = torch.zeros((2600, 304), dtype=torch.float64)  # column-major 304 x 2600
+        hBbig.t()[:300] = torch.from_numpy(B)
+        hA = hAbig.pin_memory().t()[:2500]
+        hB = hBbig.pin_memory().t()[:300]
+        assert hA.stride() == (1, 2504) and hB.stride() == (1, 304)
+        Ch = oz2.dgemm_host(hA, hB, 14, "fast").numpy()
+        Cd = oz2.dgemm(_dev(A), _dev(B), 14, "fast").cpu().numpy()
+        np.testing.assert_array_equal(Ch, Cd)
+    rng = np.random.default_rng(3)
+    ii, jj = rng.integers(0, 2500, 64), rng.integers(0, 2600, 64)
+    ref = oracle.oracle_entries(A, B, 14, "fast", ii, jj)
+    assert ulp_distance(Ch[ii, jj], ref["C"]) <= ULP_TOL
+
+
 def test_stage_timing_entry_point(oz2):
     A, B = make_matrices(256, 256, 256, 0.5, 2)
     for mode in ("fast", "accu"):
