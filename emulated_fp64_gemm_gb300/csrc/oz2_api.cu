@@ -203,8 +203,8 @@ struct DeviceState {
 };
 
 constexpr int kMaxBlocks = 8;  // row blocks of the overlapped schedule
-constexpr int kMaxParts = 2;   // column parts of its first row block
-constexpr int kMaxTasks = kMaxBlocks + kMaxParts;  // GEMM launches
+constexpr int kMaxParts = 2;   // column parts of its first (and, host entry point, last) row block
+constexpr int kMaxTasks = kMaxBlocks + 2 * kMaxParts;  // GEMM launches
 
 struct Workspace {
   size_t bytes = 0;
@@ -445,8 +445,12 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     c[n] = r;
     return n;
   };
-  int64_t cfirst[kMaxParts + 1];
+  int64_t cfirst[kMaxParts + 1], clast[kMaxParts + 1];
   const int nfirst = col_parts(fused_b ? 2 : 1, cfirst);
+  // With host buffers the last row block's GEMM is split too: the CRT and the
+  // download of its first part then run beside the GEMM of the second, which
+  // shortens the tail after the last GEMM by half a block's download.
+  const int nlast = col_parts(io ? 2 : 1, clast);
   auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
 
   // Host entry point: uploads into the staging copies A, B.  In the overlapped
@@ -607,10 +611,11 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     Task tasks[kMaxTasks];
     int ntask = 0;
     for (int b = 0; b < nb; ++b) {
-      const int np = (b == 0) ? nfirst : 1;
+      const int np = (b == 0) ? nfirst : (b == nb - 1 ? nlast : 1);
+      const int64_t* cp = (b == 0) ? cfirst : clast;
       for (int c = 0; c < np; ++c) {
-        const int64_t c0 = (np == 1) ? 0 : cfirst[c];
-        const int64_t c1 = (np == 1) ? r : cfirst[c + 1];
+        const int64_t c0 = (np == 1) ? 0 : cp[c];
+        const int64_t c1 = (np == 1) ? r : cp[c + 1];
         if (b > 0 && c == 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
         if (b_side_done && b == 0 && c == 0)
           OZ2_CU(cudaStreamWaitEvent(st, (fused_b && nfirst > 1) ? wsp->ev_bfirst : wsp->ev_bready, 0));
