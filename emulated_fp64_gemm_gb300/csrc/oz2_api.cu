@@ -419,15 +419,21 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   if (block_rows < 1024) block_rows = 1024;
   const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
   const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;
-  if (overlap) {
+  // one row block, fast mode, both sides in one read each: the two kernels run side by side
+  const bool side_by_side = pipelined && dbg == nullptr && nb == 1 && mode == OZ2_FAST &&
+                            rows_fused_fast_supported(q) && cols_fused_fast_supported(q);
+  if (overlap || side_by_side) {
     e = workspace_sync_objects(*wsp);
     if (e != OZ2_OK) return e;
   }
   const int max_bits = (hc->bound.Lbits + 1) / 2;
   bool b_side_done = false;   // B's exponents and residue planes already enqueued (on aux)
   bool b_planes_done = false;  // B's residue planes already enqueued on `stream`
-  // fast mode: B's statistics, exponents and residue planes in one read of B
+  // fast mode: B's statistics, exponents and residue planes in one read of B,
+  // and, for short rows, A's likewise
   const bool fused_b = (mode == OZ2_FAST) && cols_fused_fast_supported(q);
+  const bool fused_a = (mode == OZ2_FAST) && rows_fused_fast_supported(q);
+  bool a_planes_done = false;  // A's residue planes already enqueued on `stream` (sequential path)
   auto rows_block = [&](int64_t r0, int64_t rows) { return ScaleArgs{rows, q, r, lda, ldb, A + r0, B}; };
   // Column parts of the first row block's GEMM in the overlapped schedule: it
   // starts once B's first part is ready, and the rest of B is made beside it.
@@ -495,8 +501,12 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     // A's first-block statistics run alone first: beside B's one-read kernel
     // (which fills every SM's registers) their blocks would hardly be scheduled
     if (staged) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_upA[0], 0));
-    OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
-                                      reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    if (fused_a)
+      OZ2_CU(launch_rows_fused_fast(A, rows_of(0), q, lda, qp, p, hc->bound, hc->mod, ds->pow2mod, max_bits, alpha,
+                                    planesA, st));
+    else
+      OZ2_CU(launch_fast_exponents_rows(rows_block(0, std::min<int64_t>(block_rows, p)), hc->bound, amaxA,
+                                        reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
     OZ2_CU(cudaEventRecord(wsp->ev_start, st));
     OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
     if (fused_b) {
@@ -517,8 +527,26 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     b_side_done = true;
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
     if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
+  } else if (side_by_side) {
+    OZ2_CU(cudaEventRecord(wsp->ev_start, st));
+    OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
+    OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, r, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
+                                  wsp->aux));
+    OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
+    OZ2_CU(launch_rows_fused_fast(A, p, q, lda, qp, p, hc->bound, hc->mod, ds->pow2mod, max_bits, alpha, planesA,
+                                  st));
+    OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
+    a_planes_done = b_planes_done = true;
+    if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[2], st));
   } else if (mode == OZ2_FAST) {
-    OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    if (fused_a) {
+      OZ2_CU(launch_rows_fused_fast(A, p, q, lda, qp, p, hc->bound, hc->mod, ds->pow2mod, max_bits, alpha, planesA,
+                                    st));
+      a_planes_done = true;
+    } else {
+      OZ2_CU(launch_fast_exponents_rows(sa, hc->bound, amaxA, reinterpret_cast<uint64_t*>(at(L.sumA)), alpha, st));
+    }
     if (fused_b) {
       OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, r, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
                                     st));
@@ -574,7 +602,8 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   // CTA-pair GEMM (tcgen05 cta_group::2) unless OZ2_GEMM_1SM selects the single-SM kernel
   g.use_2sm = std::getenv("OZ2_GEMM_1SM") == nullptr;
   if (!overlap) {
-    OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
+    if (!a_planes_done)
+      OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
     if (!b_planes_done)
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
@@ -590,18 +619,24 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     cudaStream_t aux = wsp->aux;
     if (!b_side_done)
       OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
-    OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
-                                planesA, st));
+    if (!fused_a)  // (with fused_a block 0's planes came with its statistics)
+      OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
+                                  planesA, st));
     OZ2_CU(cudaEventRecord(wsp->ev_ready, st));
     OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_ready, 0));
     for (int b = 1; b < nb; ++b) {
       const int64_t r0 = b * block_rows;
       if (staged) OZ2_CU(cudaStreamWaitEvent(aux, wsp->ev_upA[b], 0));
-      if (mode == OZ2_FAST)
-        OZ2_CU(launch_fast_exponents_rows(rows_block(r0, rows_of(b)), hc->bound, amaxA + r0,
-                                          reinterpret_cast<uint64_t*>(at(L.sumA)) + r0, alpha + r0, aux));
-      OZ2_CU(launch_residues_rows(A + r0, rows_of(b), q, lda, qp, p, hc->mod, alpha + r0, ds->pow2mod,
-                                  max_bits, planesA + r0 * qp, aux));
+      if (fused_a) {
+        OZ2_CU(launch_rows_fused_fast(A + r0, rows_of(b), q, lda, qp, p, hc->bound, hc->mod, ds->pow2mod, max_bits,
+                                      alpha + r0, planesA + r0 * qp, aux));
+      } else {
+        if (mode == OZ2_FAST)
+          OZ2_CU(launch_fast_exponents_rows(rows_block(r0, rows_of(b)), hc->bound, amaxA + r0,
+                                            reinterpret_cast<uint64_t*>(at(L.sumA)) + r0, alpha + r0, aux));
+        OZ2_CU(launch_residues_rows(A + r0, rows_of(b), q, lda, qp, p, hc->mod, alpha + r0, ds->pow2mod,
+                                    max_bits, planesA + r0 * qp, aux));
+      }
       OZ2_CU(cudaEventRecord(wsp->ev_res[b], aux));
     }
     // GEMM launches on `stream`: (row block, column part)

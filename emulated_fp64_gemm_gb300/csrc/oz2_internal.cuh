@@ -128,6 +128,16 @@ cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, in
                                    const uint8_t* pow2mod, int max_bits, int32_t* beta, uint16_t* planes,
                                    cudaStream_t st);
 
+// fast mode, A side for short rows in one read of A: alpha and the residue
+// planes of `rows` rows (identical to launch_fast_exponents_rows followed by
+// launch_residues_rows); A, alpha and planes point at the first row, plane
+// rows are plane_rows apart.  For q <= 2048 only (rows_fused_fast_supported).
+bool rows_fused_fast_supported(int64_t q);
+cudaError_t launch_rows_fused_fast(const double* A, int64_t rows, int64_t q, int64_t lda, int64_t qp,
+                                   int64_t plane_rows, const BoundConsts& bc, const ModConsts& mc,
+                                   const uint8_t* pow2mod, int max_bits, int32_t* alpha, uint16_t* planes,
+                                   cudaStream_t st);
+
 // GEMM epilogue kinds
 enum GemmKind { kGemmMod = 0, kGemmExactP = 1, kGemmBound = 2 };
 

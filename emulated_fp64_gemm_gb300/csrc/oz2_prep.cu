@@ -638,6 +638,85 @@ __global__ void __launch_bounds__(256, 2) fused_cols_fast_kernel(const double* _
   }
 }
 
+// Fast mode, A side for short rows in one read of A: statistics, exponent
+// alpha_i and residue planes of R rows per block.  Thread t holds row t % R's
+// columns [8 s + 8 S c, +8) for c < 4 (s = t / R, S = 256 / R column slots), so
+// q <= 8192 / R; the per-row max and sum of squares reduce over the lanes that
+// share a row and then over the warps, with no atomics and nothing to clear.
+// Results are identical to the per-row-block path (amax_rows, sumsq_rows +
+// fast_exp, residue_rows).
+template <int R, int NW>
+__global__ void __launch_bounds__(256, 1) fused_rows_fast_kernel(const double* __restrict__ A, int64_t rows,
+                                                              int64_t q, int64_t lda, int64_t qp,
+                                                              int64_t plane_rows, BoundConsts bc, ModConsts mc,
+                                                              const uint8_t* __restrict__ pow2mod,
+                                                              int32_t* __restrict__ alpha,
+                                                              uint16_t* __restrict__ planes) {
+  constexpr int S = 256 / R;  // column slots per row
+  constexpr int NCH = 4;      // 8-column chunks per thread
+  __shared__ uint64_t red[8][R];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = tid % R, cs = tid / R;
+  const int64_t i = blockIdx.x * static_cast<int64_t>(R) + r;
+  const bool row_ok = i < rows;
+  double x[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = 8ll * cs + 8ll * S * c;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[c][k] = (row_ok && l0 + k < q) ? __ldg(A + (l0 + k) * lda + i) : 0.0;
+  }
+  // max |a| of the row (as the bits of |a|): lanes r, r + R, ... of a warp share row r
+  uint64_t m = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x[c][k])) & ~(1ull << 63);
+      m = b > m ? b : m;
+    }
+#pragma unroll
+  for (int o = R; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_xor_sync(0xffffffffu, m, o);
+    m = y > m ? y : m;
+  }
+  if (lane < R) red[warp][lane] = m;
+  __syncthreads();
+  m = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = red[w][r] > m ? red[w][r] : m;
+  __syncthreads();
+  // S_i = sum ceil(|a| 2^(F-e))^2
+  const int e = exp_of_bits(m);
+  uint64_t sum = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t cs2 = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(x[c][k])), kF - e);
+      sum += static_cast<uint64_t>(cs2) * cs2;
+    }
+#pragma unroll
+  for (int o = R; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < R) red[warp][lane] = sum;
+  __syncthreads();
+  sum = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) sum += red[w][r];
+  const int ai = (sum == 0) ? 0 : (max_shift_le_L(sum, bc) >> 1) - e + kF;
+  if (!row_ok) return;
+  if (cs == 0) alpha[i] = ai;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = 8ll * cs + 8ll * S * c;
+    if (l0 < qp) {
+      const int64_t nv = q - l0;
+      residues8<NW>(x[c], A + l0 * lda + i, lda, nv < 0 ? 0 : (nv < 8 ? static_cast<int>(nv) : 8), ai, mc,
+                    pow2mod, planes + i * qp + l0, plane_rows * qp);
+    }
+  }
+}
+
 __global__ void planes_to_int8_kernel(const uint16_t* __restrict__ planes, int64_t rows, int64_t q,
                                       int64_t qp, int s, int8_t* __restrict__ out) {
   const int64_t n = static_cast<int64_t>(s) * rows * q;
@@ -778,6 +857,26 @@ cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t 
     residue_cols_kernel<2><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
   else
     residue_cols_kernel<3><<<g, 256, 0, st>>>(B, q, r, ldb, qp, beta, mc, pow2mod, planes);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+bool rows_fused_fast_supported(int64_t q) { return q <= 2048; }
+
+cudaError_t launch_rows_fused_fast(const double* A, int64_t rows, int64_t q, int64_t lda, int64_t qp,
+                                   int64_t plane_rows, const BoundConsts& bc, const ModConsts& mc,
+                                   const uint8_t* pow2mod, int max_bits, int32_t* alpha, uint16_t* planes,
+                                   cudaStream_t st) {
+  if (!rows_fused_fast_supported(q) || rows < 1) return cudaErrorInvalidValue;
+  const int R = (qp <= 1024) ? 8 : 4;
+  const dim3 g(static_cast<unsigned>((rows + R - 1) / R));
+  if (max_bits <= 64) {
+    if (R == 8) fused_rows_fast_kernel<8, 2><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, planes);
+    else fused_rows_fast_kernel<4, 2><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, planes);
+  } else {
+    if (R == 8) fused_rows_fast_kernel<8, 3><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, planes);
+    else fused_rows_fast_kernel<4, 3><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, planes);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

@@ -48,6 +48,8 @@ WORKLOADS = {
     # preprocessing (B's one-read kernel on 2048-column parts, A's residues at q = 8192)
     "p2048_q8192_r4096_s14_fast": Workload("p2048_q8192_r4096_s14_fast", 2048, 8192, 4096, 14, "fast", 0.5, 123456),
     "n4096_s14_accu": Workload("n4096_s14_accu", 4096, 4096, 4096, 14, "accu", 1.0, 7),
+    # the pages' mid size for fast mode (paper Table 3 column n = 4096)
+    "n4096_s14_fast": Workload("n4096_s14_fast", 4096, 4096, 4096, 14, "fast", 0.5, 123456),
     "n8192_s14_fast": Workload("n8192_s14_fast", 8192, 8192, 8192, 14, "fast", 0.5, 123456),
     "n8192_s14_accu": Workload("n8192_s14_accu", 8192, 8192, 8192, 14, "accu", 0.5, 123456),
     "n8192_s18_fast": Workload("n8192_s18_fast", 8192, 8192, 8192, 18, "fast", 0.5, 123456),
