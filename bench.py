@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the native cuBLAS DGEMM timing reported as context")
     return ap.parse_args(argv)
 
 
@@ -337,6 +339,23 @@ def run_ours(args, rank, world, local):
     if clk is not None:
         extra["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                            "reasons": clk["reasons"], "samples": clk["samples"]}
+
+    # context: native FP64 GEMM (cuBLAS DGEMM through torch.matmul, a library call) on the
+    # same device-resident operands, the comparison the pages' tables make
+    if not args.no_context:
+        ref = torch.matmul(dA, dB)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        c0.record(stream)
+        for _ in range(reps):
+            torch.matmul(dA, dB, out=ref)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        dg_ms = c0.elapsed_time(c1) / reps
+        extra["context"] = {"cublas_dgemm_tflops": w.flops / dg_ms / 1e9, "cublas_dgemm_ms": dg_ms,
+                            "note": "native FP64 GEMM on the same operands (torch.matmul, float64)"}
+        del ref
 
     # end to end through the host-memory entry point: H2D of A and B, D2H of C
     if not args.no_e2e:

@@ -226,6 +226,20 @@ def test_host_entry_point_staged_uploads(oz2):
     assert ulp_distance(Ch[ii, jj], ref["C"]) <= ULP_TOL
 
 
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+def test_single_cta_gemm_selection_matches(oz2, mode, monkeypatch):
+    """OZ2_GEMM_1SM=1 selects the single-CTA tcgen05 kernel for the modular and
+    bound GEMMs (read per call); it must give the CTA-pair kernel's C bit for bit."""
+    A, B = make_matrices(700, 600, 530, 1.0, 91)
+    dA, dB = _dev(A), _dev(B)
+    C2 = oz2.dgemm(dA, dB, 14, mode).cpu().numpy()
+    monkeypatch.setenv("OZ2_GEMM_1SM", "1")
+    C1 = oz2.dgemm(dA, dB, 14, mode).cpu().numpy()
+    monkeypatch.delenv("OZ2_GEMM_1SM")
+    np.testing.assert_array_equal(C1, C2)
+    assert oz2.last_error() == 0
+
+
 def test_stage_timing_entry_point(oz2):
     A, B = make_matrices(256, 256, 256, 0.5, 2)
     for mode in ("fast", "accu"):
