@@ -417,6 +417,13 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   int64_t block_rows = (p + 3) / 4;
   block_rows = (block_rows + 255) / 256 * 256;  // whole 256-row pair tiles
   if (block_rows < 1024) block_rows = 1024;
+  // Small products run as one block: below about 2^35 multiply-adds in fast
+  // mode (2^32 in accu mode) the extra launches and cross-stream waits of the
+  // overlapped schedule cost more than the work they hide (measured 3-15 %
+  // on 1536- to 4096-row shapes).  The host entry point keeps its blocks,
+  // which also stage its uploads.
+  const double work = static_cast<double>(p) * static_cast<double>(q) * static_cast<double>(r);
+  if (io == nullptr && work < (mode == OZ2_FAST ? 0x1p35 : 0x1p32)) block_rows = p;
   const int nb = static_cast<int>((p + block_rows - 1) / block_rows);
   const bool overlap = pipelined && dbg == nullptr && nb > 1 && nb <= kMaxBlocks;
   // one row block, fast mode, both sides in one read each: the two kernels run side by side

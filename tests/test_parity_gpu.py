@@ -296,24 +296,46 @@ def test_full_size_workloads_sampled(oz2, name):
     _sampled_check(oz2, name)
 
 
+# Products below 2^35 multiply-adds in fast mode (2^32 in accu mode) run as one
+# row block; these shapes sit above those sizes so that the overlapped
+# schedule runs.
+OVERLAP_SHAPES = {"fast": (2500, 5600, 2500), "accu": (2500, 900, 2000)}
+
+
+def _sampled_entries(p, r, seed, extra_i=(), extra_j=()):
+    rng = np.random.default_rng(seed)
+    ii = np.concatenate([rng.integers(0, p, 200), [0, p - 1, *extra_i]])
+    jj = np.concatenate([rng.integers(0, r, 200), [r - 1, 0, *extra_j]])
+    return ii.astype(np.int64), jj.astype(np.int64)
+
+
 @pytest.mark.parametrize("mode", ["fast", "accu"])
 def test_overlapped_row_blocks_match_sequential(oz2, mode):
     """p = 2500 gives three row blocks (1024, 1024, 452) in the overlapped schedule."""
-    A, B = make_matrices(2500, 300, 200, 1.0, 77)
+    p, q, r = OVERLAP_SHAPES[mode]
+    assert p * q * r >= (2**35 if mode == "fast" else 2**32)
+    A, B = make_matrices(p, q, r, 1.0, 77)
     dA, dB = _dev(A), _dev(B)
     got = oz2.dgemm_debug(dA, dB, 14, mode, want_p=False)  # stages one after another
     C = oz2.dgemm(dA, dB, 14, mode)                          # overlapped row blocks
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(C.cpu().numpy(), got["C"].cpu().numpy())
-    ref = oracle.oracle_dgemm(A, B, 14, mode)
-    assert ulp_distance(C.cpu().numpy(), ref["C"]) <= ULP_TOL
-    np.testing.assert_array_equal(got["R"].cpu().numpy(), np.transpose(ref["R"], (0, 2, 1)))
+    Cn = C.cpu().numpy()
+    np.testing.assert_array_equal(Cn, got["C"].cpu().numpy())
+    ref_a, ref_b, _ = oracle.exponents(A, B, 14, mode)
+    np.testing.assert_array_equal(got["alpha"].cpu().numpy(), ref_a)
+    np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref_b)
+    ii, jj = _sampled_entries(p, r, 6, [1023, 1024, 2047, 2048], [1, 2, 3, 4])
+    ref = oracle.oracle_entries(A, B, 14, mode, ii, jj, alpha=ref_a, beta=ref_b)
+    assert ulp_distance(Cn[ii, jj], ref["C"]) <= ULP_TOL
+    Rn = got["R"].cpu().numpy()  # [s][r][p]
+    np.testing.assert_array_equal(Rn[:, jj, ii], ref["R"])
 
 
 def test_overlapped_first_block_column_parts(oz2):
-    """r = 2600: the first row block's GEMM runs as two column parts (0..1535,
-    1536..2599), the first starting once B's first columns are ready."""
-    A, B = make_matrices(2500, 200, 2600, 0.5, 78)
+    """r = 2500: the first row block's GEMM runs as two column parts (0..1535,
+    1536..2499), the first starting once B's first columns are ready."""
+    p, q, r = OVERLAP_SHAPES["fast"]
+    A, B = make_matrices(p, q, r, 0.5, 78)
     dA, dB = _dev(A), _dev(B)
     got = oz2.dgemm_debug(dA, dB, 14, "fast", want_p=False)  # stages one after another
     C = oz2.dgemm(dA, dB, 14, "fast")                          # overlapped schedule
@@ -324,9 +346,7 @@ def test_overlapped_first_block_column_parts(oz2):
     ref_a, ref_b, _ = oracle.exponents(A, B, 14, "fast")
     np.testing.assert_array_equal(alpha, ref_a)
     np.testing.assert_array_equal(beta, ref_b)
-    rng = np.random.default_rng(5)
-    ii = np.concatenate([rng.integers(0, 2500, 200), [0, 1023, 1024, 2499]])
-    jj = np.concatenate([rng.integers(0, 2600, 200), [1535, 1536, 0, 2599]])
+    ii, jj = _sampled_entries(p, r, 5, [1023, 1024], [1535, 1536])
     ref = oracle.oracle_entries(A, B, 14, "fast", ii, jj, alpha=ref_a, beta=ref_b)
     assert ulp_distance(Cn[ii, jj], ref["C"]) <= ULP_TOL
 
