@@ -203,7 +203,7 @@ struct DeviceState {
 };
 
 constexpr int kMaxBlocks = 8;  // row blocks of the overlapped schedule
-constexpr int kMaxParts = 2;   // column parts of its first (and, host entry point, last) row block
+constexpr int kMaxParts = 4;   // column parts of its first (and, host entry point, last) row block
 constexpr int kMaxTasks = kMaxBlocks + 2 * kMaxParts;  // GEMM launches
 
 struct Workspace {
@@ -214,7 +214,7 @@ struct Workspace {
   cudaEvent_t ev_ready = nullptr;
   cudaEvent_t ev_res[kMaxBlocks] = {};
   cudaEvent_t ev_gemm[kMaxTasks] = {};
-  cudaEvent_t ev_bfirst = nullptr;
+  cudaEvent_t ev_bpart[kMaxParts] = {};  // B's planes of each first-block column part made
   cudaEvent_t ev_done = nullptr;
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_bready = nullptr;
@@ -307,9 +307,9 @@ oz2_status workspace_sync_objects(Workspace& w) {
   if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   if (cudaStreamCreateWithFlags(&w.up, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_bfirst) && mk(&w.ev_io);
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_io);
   for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_upA[b]);
-  for (int c = 0; c < kMaxParts; ++c) ok = ok && mk(&w.ev_upB[c]);
+  for (int c = 0; c < kMaxParts; ++c) ok = ok && mk(&w.ev_upB[c]) && mk(&w.ev_bpart[c]);
   for (int t = 0; t < kMaxTasks; ++t) ok = ok && mk(&w.ev_gemm[t]);
   return ok ? OZ2_OK : OZ2_ERR_CUDA;
 }
@@ -445,13 +445,14 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   // Column parts of the first row block's GEMM in the overlapped schedule: it
   // starts once B's first part is ready, and the rest of B is made beside it.
   // Parts are whole multiples of 512 columns (pairs of 256-column tiles); at
-  // most `want` of them.  (Splitting the last block too, so that the CRT of
-  // its first parts overlaps the GEMM of the rest, measured slower: the extra
-  // GEMM launches cost more than the hidden CRT.)
+  // most `want` of them.  (In the device entry point, splitting the last block
+  // too, so that the CRT of its first parts overlaps the GEMM of the rest,
+  // measured slower: the extra GEMM launches cost more than the hidden CRT.)
   auto col_parts = [&](int want, int64_t* c) {
     c[0] = 0;
     c[1] = r;
-    if (want < 2 || r < 1024ll * want) return 1;
+    if (want > r / 1024) want = static_cast<int>(r / 1024);  // parts of at least 1024 columns
+    if (want < 2) return 1;
     const int64_t w = (r / want + 511) / 512 * 512;
     int n = 0;
     for (int64_t c0 = 0; c0 < r; c0 += w) c[n++] = c0;
@@ -459,11 +460,13 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     return n;
   };
   int64_t cfirst[kMaxParts + 1], clast[kMaxParts + 1];
-  const int nfirst = col_parts(fused_b ? 2 : 1, cfirst);
-  // With host buffers the last row block's GEMM is split too: the CRT and the
-  // download of its first part then run beside the GEMM of the second, which
-  // shortens the tail after the last GEMM by half a block's download.
-  const int nlast = col_parts(io ? 2 : 1, clast);
+  // (host entry point: four parts, so that the first GEMM waits for a quarter
+  // of B's upload instead of half)
+  const int nfirst = col_parts(fused_b ? (io ? 4 : 2) : 1, cfirst);
+  // With host buffers the last row block's GEMM is split too (four parts): the
+  // CRT and the download of each part then run beside the GEMM of the next,
+  // which leaves a quarter of a block's download after the last GEMM.
+  const int nlast = col_parts(io ? 4 : 1, clast);
   auto rows_of = [&](int b) { return std::min<int64_t>(block_rows, p - b * block_rows); };
 
   // Host entry point: uploads into the staging copies A, B.  In the overlapped
@@ -522,7 +525,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
         if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[c], 0));
         OZ2_CU(launch_cols_fused_fast(B + c0 * ldb, q, cfirst[c + 1] - c0, ldb, qp, r, hc->bound, hc->mod,
                                       ds->pow2mod, max_bits, beta + c0, planesB + c0 * qp, wsp->aux));
-        if (c == 0) OZ2_CU(cudaEventRecord(wsp->ev_bfirst, wsp->aux));
+        OZ2_CU(cudaEventRecord(wsp->ev_bpart[c], wsp->aux));
       }
     } else {
       if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[0], 0));  // one part: all of B
@@ -659,9 +662,9 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
         const int64_t c0 = (np == 1) ? 0 : cp[c];
         const int64_t c1 = (np == 1) ? r : cp[c + 1];
         if (b > 0 && c == 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
-        if (b_side_done && b == 0 && c == 0)
-          OZ2_CU(cudaStreamWaitEvent(st, (fused_b && nfirst > 1) ? wsp->ev_bfirst : wsp->ev_bready, 0));
-        if (b_side_done && b == 0 && c == 1) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_bready, 0));
+        // block 0's part c waits for B's part c (one part: for all of B)
+        if (b_side_done && b == 0)
+          OZ2_CU(cudaStreamWaitEvent(st, (fused_b && nfirst > 1) ? wsp->ev_bpart[c] : wsp->ev_bready, 0));
         if (ntask == 0 && ev) OZ2_CU(cudaEventRecord(ev[3], st));
         g.row0 = b * block_rows;
         g.p = rows_of(b);

@@ -226,6 +226,23 @@ def test_host_entry_point_staged_uploads(oz2):
     assert ulp_distance(Ch[ii, jj], ref["C"]) <= ULP_TOL
 
 
+def test_host_entry_point_four_column_parts(oz2):
+    """r = 6000: the host entry point uploads B in four column parts (0, 1536,
+    3072, 4608) and splits the first and last row blocks' GEMMs the same way,
+    each part's CRT and download running beside the next part's GEMM."""
+    A, B = make_matrices(2500, 300, 6000, 0.5, 83)
+    hA = torch.from_numpy(np.asfortranarray(A)).pin_memory()
+    hB = torch.from_numpy(np.asfortranarray(B)).pin_memory()
+    Ch = oz2.dgemm_host(hA, hB, 14, "fast").numpy()
+    Cd = oz2.dgemm(_dev(A), _dev(B), 14, "fast").cpu().numpy()
+    np.testing.assert_array_equal(Ch, Cd)
+    rng = np.random.default_rng(4)
+    ii = np.concatenate([rng.integers(0, 2500, 100), [0, 1023, 1024, 2047, 2048, 2499]])
+    jj = np.concatenate([rng.integers(0, 6000, 100), [1535, 1536, 3071, 3072, 4607, 4608]])
+    ref = oracle.oracle_entries(A, B, 14, "fast", ii, jj)
+    assert ulp_distance(Ch[ii, jj], ref["C"]) <= ULP_TOL
+
+
 @pytest.mark.parametrize("mode", ["fast", "accu"])
 def test_single_cta_gemm_selection_matches(oz2, mode, monkeypatch):
     """OZ2_GEMM_1SM=1 selects the single-CTA tcgen05 kernel for the modular and
