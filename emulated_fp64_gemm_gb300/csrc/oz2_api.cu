@@ -211,6 +211,11 @@ struct Workspace {
   uint8_t* base = nullptr;
   // second stream and events of the overlapped schedule (created on first use)
   cudaStream_t aux = nullptr;
+  // the overlapped schedule's GEMM launches, at the device's greatest stream
+  // priority, so that the block scheduler places a GEMM's CTAs before the
+  // blocks of a side kernel that became ready at the same moment
+  cudaStream_t gemm = nullptr;
+  cudaEvent_t ev_gemm_go = nullptr;
   cudaEvent_t ev_ready = nullptr;
   cudaEvent_t ev_res[kMaxBlocks] = {};
   cudaEvent_t ev_gemm[kMaxTasks] = {};
@@ -306,8 +311,11 @@ oz2_status workspace_sync_objects(Workspace& w) {
   if (w.aux) return OZ2_OK;
   if (cudaStreamCreateWithFlags(&w.aux, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
   if (cudaStreamCreateWithFlags(&w.up, cudaStreamNonBlocking) != cudaSuccess) return OZ2_ERR_CUDA;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return OZ2_ERR_CUDA;
+  if (cudaStreamCreateWithPriority(&w.gemm, cudaStreamNonBlocking, greatest) != cudaSuccess) return OZ2_ERR_CUDA;
   auto mk = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_io);
+  bool ok = mk(&w.ev_ready) && mk(&w.ev_done) && mk(&w.ev_start) && mk(&w.ev_bready) && mk(&w.ev_io) && mk(&w.ev_gemm_go);
   for (int b = 0; b < kMaxBlocks; ++b) ok = ok && mk(&w.ev_res[b]) && mk(&w.ev_upA[b]);
   for (int c = 0; c < kMaxParts; ++c) ok = ok && mk(&w.ev_upB[c]) && mk(&w.ev_bpart[c]);
   for (int t = 0; t < kMaxTasks; ++t) ok = ok && mk(&w.ev_gemm[t]);
@@ -649,7 +657,14 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
       }
       OZ2_CU(cudaEventRecord(wsp->ev_res[b], aux));
     }
-    // GEMM launches on `stream`: (row block, column part)
+    // GEMM launches, (row block, column part), on the greatest-priority
+    // stream.  When a GEMM launch ends, the next one and the CRT of the one
+    // that ended become ready together; at equal priority the CRT's blocks
+    // could take every SM first, and the next GEMM's CTAs (which need almost
+    // all of an SM's shared memory) then waited for the whole CRT.
+    cudaStream_t gs = wsp->gemm;
+    OZ2_CU(cudaEventRecord(wsp->ev_gemm_go, st));  // after block 0's residues (and statistics)
+    OZ2_CU(cudaStreamWaitEvent(gs, wsp->ev_gemm_go, 0));
     struct Task {
       int64_t row0, rows, col0, cols;
     };
@@ -661,21 +676,21 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
       for (int c = 0; c < np; ++c) {
         const int64_t c0 = (np == 1) ? 0 : cp[c];
         const int64_t c1 = (np == 1) ? r : cp[c + 1];
-        if (b > 0 && c == 0) OZ2_CU(cudaStreamWaitEvent(st, wsp->ev_res[b], 0));
+        if (b > 0 && c == 0) OZ2_CU(cudaStreamWaitEvent(gs, wsp->ev_res[b], 0));
         // block 0's part c waits for B's part c (one part: for all of B)
         if (b_side_done && b == 0)
-          OZ2_CU(cudaStreamWaitEvent(st, (fused_b && nfirst > 1) ? wsp->ev_bpart[c] : wsp->ev_bready, 0));
-        if (ntask == 0 && ev) OZ2_CU(cudaEventRecord(ev[3], st));
+          OZ2_CU(cudaStreamWaitEvent(gs, (fused_b && nfirst > 1) ? wsp->ev_bpart[c] : wsp->ev_bready, 0));
+        if (ntask == 0 && ev) OZ2_CU(cudaEventRecord(ev[3], gs));
         g.row0 = b * block_rows;
         g.p = rows_of(b);
         g.col0 = c0;
         g.ncols = c1 - c0;
-        OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, st));
-        OZ2_CU(cudaEventRecord(wsp->ev_gemm[ntask], st));
+        OZ2_CU(launch_gemm(kGemmMod, g, hc->mod, gs));
+        OZ2_CU(cudaEventRecord(wsp->ev_gemm[ntask], gs));
         tasks[ntask++] = Task{g.row0, g.p, c0, c1 - c0};
       }
     }
-    if (ev) OZ2_CU(cudaEventRecord(ev[4], st));
+    if (ev) OZ2_CU(cudaEventRecord(ev[4], gs));
     // CRT (and download) of each launch's output on the second stream
     for (int t = 0; t < ntask; ++t) {
       const Task& k = tasks[t];

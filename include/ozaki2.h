@@ -23,9 +23,14 @@
  * (there are no BLAS alpha/beta scalars).  A, B and C are caller-owned device
  * memory (ozaki2_dgemm_host excepted) and C must not overlap A or B.
  *
- * Asynchrony: ozaki2_dgemm enqueues all its kernels on `stream` (a
- * cudaStream_t; NULL means the legacy default stream) and returns without
- * synchronising.  Argument errors are returned before anything is enqueued.
+ * Asynchrony: ozaki2_dgemm is ordered after earlier work on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream), later work on
+ * `stream` is ordered after it, and it returns without synchronising.
+ * Inside, the overlapped schedule also runs kernels on two library-owned
+ * streams of the same workspace, joined to `stream` by events: a second
+ * stream for preprocessing and the CRT, and a stream at the device's
+ * greatest priority for the GEMMs.  Argument errors are returned before
+ * anything is enqueued.
  *
  * Workspace: intermediate planes, residues and exponents live in a
  * library-owned device workspace, one per (device, stream) pair, grown on
