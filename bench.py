@@ -144,6 +144,55 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def cublas_emulated_dgemm_ms(dA, dB, dC, p, q, r, stream, reps):
+    """Time cuBLAS's own fixed-point FP64 emulation (compute type
+    CUBLAS_COMPUTE_64F_EMULATED_FIXEDPOINT, emulation math mode, eager
+    strategy) on the same column-major operands, as context.  A library call
+    through ctypes; returns (ms per call, None) or (None, reason)."""
+    import ctypes
+
+    import torch
+    cb = None
+    for name in ("libcublas.so.13", "/usr/local/cuda/lib64/libcublas.so.13"):
+        try:
+            cb = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if cb is None:
+        return None, "libcublas.so.13 not found"
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    h = vp()
+    if cb.cublasCreate_v2(ctypes.byref(h)) != 0:
+        return None, "cublasCreate failed"
+    try:
+        cb.cublasGemmEx.argtypes = [vp, ci, ci, ci, ci, ci, vp, vp, ci, ci, vp, ci, ci, vp, vp, ci, ci, ci, ci]
+        one, zero = ctypes.c_double(1.0), ctypes.c_double(0.0)
+        CUDA_R_64F, COMPUTE_64F_EMULATED_FIXEDPOINT, FP64_EMULATED_FIXEDPOINT_MATH, EAGER = 1, 79, 8, 2
+        if (cb.cublasSetStream_v2(h, vp(stream.cuda_stream)) != 0
+                or cb.cublasSetMathMode(h, FP64_EMULATED_FIXEDPOINT_MATH) != 0
+                or cb.cublasSetEmulationStrategy(h, EAGER) != 0):
+            return None, "cuBLAS emulation settings refused"
+
+        def call():
+            return cb.cublasGemmEx(h, 0, 0, p, r, q, ctypes.cast(ctypes.byref(one), vp), vp(dA.data_ptr()),
+                                   CUDA_R_64F, p, vp(dB.data_ptr()), CUDA_R_64F, q,
+                                   ctypes.cast(ctypes.byref(zero), vp), vp(dC.data_ptr()), CUDA_R_64F, p,
+                                   COMPUTE_64F_EMULATED_FIXEDPOINT, -1)
+        if call() != 0:
+            return None, "cublasGemmEx with the emulated compute type failed"
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(reps):
+            call()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / reps, None
+    finally:
+        cb.cublasDestroy_v2(h)
+
+
 def dist_setup():
     """(rank, world, local_rank); initialises torch.distributed under torchrun."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -355,7 +404,18 @@ def run_ours(args, rank, world, local):
         dg_ms = c0.elapsed_time(c1) / reps
         extra["context"] = {"cublas_dgemm_tflops": w.flops / dg_ms / 1e9, "cublas_dgemm_ms": dg_ms,
                             "note": "native FP64 GEMM on the same operands (torch.matmul, float64)"}
-        del ref
+        # cuBLAS's fixed-point FP64 emulation on the same operands (C column-major, ldc = p)
+        dCe = torch.empty((w.r, w.p), dtype=torch.float64, device=dA.device).t()
+        em_ms, why = cublas_emulated_dgemm_ms(dA, dB, dCe, w.p, w.q, w.r, stream, reps)
+        if em_ms is None:
+            extra["context"]["cublas_fp64_emulated"] = {"unavailable": why}
+        else:
+            extra["context"]["cublas_fp64_emulated"] = {
+                "tflops": w.flops / em_ms / 1e9, "ms": em_ms,
+                "note": ("cublasGemmEx, CUBLAS_COMPUTE_64F_EMULATED_FIXEDPOINT, emulation math mode, "
+                         "eager strategy; a rate equal to the native DGEMM's means the emulation "
+                         "did not engage on this device")}
+        del ref, dCe
 
     # end to end through the host-memory entry point: H2D of A and B, D2H of C
     if not args.no_e2e:

@@ -130,16 +130,18 @@ __device__ __forceinline__ uint64_t warp_column_max(uint64_t (&kc)[32], int lane
 // int32 running sums held BNc columns further on in tensor memory.  After the
 // last chunk each entry W_ij of the row becomes the order-preserving keys of
 // W 2^-v_j (row maximum) and W 2^-u_i (column maximum over the warp's 32 rows),
-// and the maxima are taken with 64-bit atomics.
+// and the maxima are taken with 64-bit atomics.  The thread handles the
+// 32-column blocks [cb0, cb1) of the slot.
 template <int BNc>
 __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, bool last, int64_t il, int64_t i,
-                                                     int64_t j0, int lane, const KParams& kp) {
+                                                     int64_t j0, int lane, const KParams& kp, int cb0 = 0,
+                                                     int cb1 = BNc / 32) {
   const uint32_t sum_addr = acc_addr + BNc;
   const bool row_ok = il < kp.p;
   const int ui = (last && row_ok) ? kp.u[i] : 0;
   uint64_t rmax = 0;
 #pragma unroll 1
-  for (int cb = 0; cb < BNc / 32; ++cb) {
+  for (int cb = cb0; cb < cb1; ++cb) {
     uint32_t v[32], sacc[32];
     tmem_ld32(acc_addr + cb * 32, v);
     if (c > 0) tmem_ld32(sum_addr + cb * 32, sacc);
@@ -174,6 +176,56 @@ __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, b
   if (last && rmax)
     atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), static_cast<unsigned long long>(rmax));
   if (!last) tmem_wait_st();
+}
+
+// CTA-pair bound GEMM, after the last chunk has been added into the running
+// sums (which then hold W itself, read here from sum_addr): the row maximum
+// of W 2^-v_j and the column maxima of W 2^-u_i over the warp's 32 rows, for
+// the 32-column blocks [cb0, cb1).  The keys are those of dyadic_key as a pair
+// of words, exponent word (floor(log2 value) + 4096, positive for every
+// nonzero entry) and normalised mantissa, compared lexicographically; a
+// column maximum is two 32-bit warp max reductions, first over the exponent
+// words, then over the mantissas of the lanes that hold that exponent.  The
+// tensor core is already working on the next unit's accumulator meanwhile.
+__device__ __forceinline__ void bound_final_keys2(uint32_t sum_addr, int64_t il, int64_t i, int64_t j0, int lane,
+                                                  const KParams& kp, int cb0, int cb1) {
+  const bool row_ok = il < kp.p;
+  const int ui = row_ok ? kp.u[i] : 0;
+  uint32_t rhi = 0, rlo = 0;
+#pragma unroll 1
+  for (int cb = cb0; cb < cb1; ++cb) {
+    uint32_t w[32];
+    tmem_ld32(sum_addr + cb * 32, w);
+    const int64_t jl = j0 + cb * 32 + lane;  // this lane's column
+    const int vl = (jl < kp.r) ? kp.v[jl] : 0;
+    tmem_wait_ld();
+    uint32_t chi = 0, clo = 0;  // the maximum of column jl
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int64_t j = j0 + cb * 32 + k;
+      const uint32_t x = (row_ok && j < kp.r) ? w[k] : 0u;
+      const int vj = __shfl_sync(0xffffffffu, vl, k);
+      const int b = 32 - __clz(static_cast<int>(x));  // bit length (0 for x = 0)
+      const uint32_t mant = x ? (x << (32 - b)) : 0u;
+      const uint32_t hr = x ? static_cast<uint32_t>(b - 1 - vj + 4096) : 0u;
+      const uint32_t hc = x ? static_cast<uint32_t>(b - 1 - ui + 4096) : 0u;
+      if (hr > rhi || (hr == rhi && mant > rlo)) {
+        rhi = hr;
+        rlo = mant;
+      }
+      const uint32_t mh = __reduce_max_sync(0xffffffffu, hc);
+      const uint32_t ml = __reduce_max_sync(0xffffffffu, hc == mh ? mant : 0u);
+      if (lane == k) {
+        chi = mh;
+        clo = ml;
+      }
+    }
+    if ((chi | clo) != 0 && jl < kp.r)
+      atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + jl),
+                (static_cast<unsigned long long>(chi) << 32) | clo);
+  }
+  if ((rhi | rlo) != 0)
+    atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), (static_cast<unsigned long long>(rhi) << 32) | rlo);
 }
 
 // First K block of chunk c: the nkb blocks are split into nchunks chunks of
@@ -514,9 +566,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // leader's "full" barriers, the MMA commits are multicast to both CTAs, and
 // both epilogues signal the leader's "empty accumulator" barriers.  The chunk
 // schedule and the in-place reduction are those of the single-SM kernel.
-// BN2 = 256 columns per tile for the modular GEMMs; 128 for the accu bound
-// GEMM, whose TMEM slots also hold an int32 running sum beside the
-// accumulator (columns [256 sl, +128) and [256 sl + 128, +128)).
+// BN2 = 256 columns per tile.  A modular GEMM unit is two tiles side by side
+// (TMEM slots at columns 0 and 256), so one slot's epilogue runs while the
+// tensor core works on the other.  A unit of the accu bound GEMM is one tile:
+// its int32 running sum takes the other 256 columns (the accumulator in
+// [0, 256), the sum in [256, 512)), so the MMA waits for each chunk's
+// epilogue.  That costs less than 128-column tiles, which ran the tensor
+// core at about half its rate (the modular GEMM with 128-column tiles: 14.9
+// instead of 8.1 ms at n = 8192, s = 14).
 template <int BN2>
 struct Cfg2 {
   static constexpr int BN = BN2;                             // output columns per tile
@@ -608,6 +665,8 @@ struct Unit2 {
   int t, mp, tn0, ntile;  // channel, 256-row pair tile, first 256-column tile, tiles (1 or 2)
 };
 
+// SINGLE: one column tile per unit (kp.pairs_n then counts tiles)
+template <bool SINGLE>
 __device__ __forceinline__ Unit2 decode_unit2(int64_t u, const KParams& kp) {
   // kp.tiles_m counts 256-row pair tiles here
   const int64_t upp = static_cast<int64_t>(kp.tiles_m) * kp.pairs_n;
@@ -622,13 +681,22 @@ __device__ __forceinline__ Unit2 decode_unit2(int64_t u, const KParams& kp) {
   const int rows_in_group = static_cast<int>(left < GM ? left : GM);
   U.mp = static_cast<int>(g * GM + idx % rows_in_group);
   const int pn = static_cast<int>(idx / rows_in_group);
-  U.tn0 = pn * 2;
-  U.ntile = (U.tn0 + 1 < kp.tiles_n) ? 2 : 1;
+  U.tn0 = SINGLE ? pn : pn * 2;
+  U.ntile = (!SINGLE && U.tn0 + 1 < kp.tiles_n) ? 2 : 1;
   return U;
 }
 
+// Epilogue warps of the CTA-pair kernel: four for the modular GEMMs (one per
+// TMEM lane quadrant); eight for the bound GEMM, two per quadrant, each taking
+// half of a slot's columns, because its final epilogue (dyadic keys, column
+// maxima by shuffles, atomics) is latency-bound with one warp per scheduler.
+template <int KIND>
+__host__ __device__ constexpr int epi_warps2() {
+  return KIND == kGemmBound ? 8 : 4;
+}
+
 template <int BN2, int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2<KIND>(), 1)
     oz2_gemm2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ KParams kp) {
   using C2 = Cfg2<BN2>;
@@ -662,7 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&accf[i]), 1);
-      mbar_init(smem_u32(&acce[i]), 8);  // one elected lane per epilogue warp, 4 warps x 2 CTAs
+      mbar_init(smem_u32(&acce[i]), 2 * epi_warps2<KIND>());  // one elected lane per epilogue warp, both CTAs
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -693,7 +761,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
-        const Unit2 U = decode_unit2(u, kp);
+        const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
         const int arow = static_cast<int>(kp.row0) + U.mp * 256 + static_cast<int>(rank) * 128;
         for (int c = 0; c < kp.nchunks && ok; ++c) {
           const int kb0 = chunk_begin(c, kp);
@@ -734,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t use[2] = {0, 0};
       bool ok = true;
       for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
-        const Unit2 U = decode_unit2(u, kp);
+        const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
         for (int c = 0; c < kp.nchunks && ok; ++c) {
           const int kb0 = chunk_begin(c, kp);
           const int kb1 = chunk_begin(c + 1, kp);
@@ -778,14 +846,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_wait_bounded(smem_u32(drain), 0, abort_flag, kWaitLimitNs);
     }
   } else {
-    // ---------------------------------------------------------- epilogue (warps 2..5, both CTAs)
-    const int quad = warp & 3;
+    // ---------------------------------------------------------- epilogue (warps 2.., both CTAs)
+    const int quad = warp & 3;  // the TMEM lane quadrant this warp may access
+    constexpr int NPART = epi_warps2<KIND>() / 4;
+    const int part = (warp - 2) >> 2;  // column part of each slot (bound GEMM: two)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t use[2] = {0, 0};
     bool ok = true;
     for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
-      const Unit2 U = decode_unit2(u, kp);
+      const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
       const int64_t il = static_cast<int64_t>(U.mp) * 256 + rank * 128 + row_in_tile;
       const int64_t i = kp.row0 + il;
       const float mf = kp.mf[U.t];
@@ -804,7 +874,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
           const int64_t j0 = kp.col0 + static_cast<int64_t>(U.tn0 + sl) * BN;
           if (KIND == kGemmBound) {
-            bound_epilogue_chunk<BN>(acc_addr, c, last, il, i, j0, lane, kp);
+            // every chunk, the last included: its sums into the int32 running
+            // sums; then the accumulator goes back to the MMA, and after the
+            // last chunk the keys are taken from the running sums (= W)
+            const int cb0 = part * (BN / 32 / NPART), cb1 = (part + 1) * (BN / 32 / NPART);
+            bound_epilogue_chunk<BN>(acc_addr, c, false, il, i, j0, lane, kp, cb0, cb1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&acce[sl]), 0));
+            if (last) bound_final_keys2(acc_addr + BN, il, i, j0, lane, kp, cb0, cb1);
+            continue;
           } else if (!last) {
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
@@ -951,7 +1030,7 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   kp.col0 = g.col0;
   const int64_t ncols = g.ncols ? g.ncols : g.r;
   kp.tiles_n = static_cast<int>((ncols + BN2 - 1) / BN2);
-  kp.pairs_n = (kp.tiles_n + 1) / 2;
+  kp.pairs_n = (KIND == kGemmBound) ? kp.tiles_n : (kp.tiles_n + 1) / 2;  // bound: one tile per unit
   kp.units = static_cast<int64_t>(g.s) * kp.tiles_m * kp.pairs_n;
   kp.R = g.R;
   kp.rowkey = g.rowkey;
@@ -969,7 +1048,7 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   if (e != cudaSuccess) return e;
   int64_t clusters = std::min<int64_t>(kp.units, g.num_sms / 2);
   if (clusters < 1) clusters = 1;
-  kern<<<static_cast<unsigned>(2 * clusters), NUM_THREADS, C2::SMEM, st>>>(ta, tb, kp);
+  kern<<<static_cast<unsigned>(2 * clusters), 64 + 32 * epi_warps2<KIND>(), C2::SMEM, st>>>(ta, tb, kp);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -984,7 +1063,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmArgs& g, const ModConsts& mc, c
     case kGemmExactP:
       return launch_impl<128, kGemmExactP>(g, mc, st);
     case kGemmBound:
-      if (g.use_2sm) return launch_2sm<128, kGemmBound>(g, mc, st);
+      if (g.use_2sm) return launch_2sm<256, kGemmBound>(g, mc, st);
       return launch_impl<128, kGemmBound>(g, mc, st);
   }
   return cudaErrorInvalidValue;
