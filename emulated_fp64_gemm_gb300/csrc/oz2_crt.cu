@@ -165,8 +165,9 @@ __device__ __forceinline__ double crt_round_x(uint32_t (&X)[NL], const CrtConsts
 // Output rows [row0, row0 + rows).  W holds the coefficients as
 // [s][r4][p_total][4] (four consecutive columns of one row per word); X has
 // p_total rows per column.  Thread = (row i, group of 4 columns); x walks the
-// rows, y a strided set of column groups.
-template <int MAXS, int NL16>
+// rows, y a strided set of column groups.  NBC: the byte limbs of the largest
+// M/m_t for s <= MAXS (s - 1 for s >= 5); the dp4a loop stops there.
+template <int MAXS, int NL16, int NBC>
 __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
                                                   int64_t jg0, int64_t jg1, int64_t r,
                                                   const __grid_constant__ CrtConsts cc,
@@ -185,7 +186,8 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, in
   for (int64_t jg = jg0 + blockIdx.y; jg < jg1; jg += gridDim.y) {
     const int64_t base = jg * p_total + i;
     constexpr int NG = (MAXS + 3) / 4;  // channel groups of four
-    constexpr int NB8 = 2 * NL16;       // byte limbs
+    constexpr int NB8 = 2 * NL16;       // byte limbs of the sums
+    static_assert(NBC <= NB8, "coefficient bytes within the sum's limbs");
     uint32_t wv[4 * NG];
 #pragma unroll
     for (int t = 0; t < 4 * NG; ++t) wv[t] = (t < cc.s) ? __ldg(W + t * plane + base) : 0u;
@@ -201,32 +203,53 @@ __global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, in
       wv[4 * g + 2] = __byte_perm(hi01, hi23, 0x5410u);
       wv[4 * g + 3] = __byte_perm(hi01, hi23, 0x7632u);
     }
-#pragma unroll 1
-    for (int v = 0; v < 4; ++v) {
+    // one output column v of the four, from its coefficient word of each group
+    auto one_output = [&](int v, const uint32_t (&wsel)[NG]) {
       const int64_t j = jg * 4 + v;
-      if (j >= r) break;
       // Y in byte limbs: S_b = sum_t w_t byte_b(M/m_t), four channels per dp4a (S_b < 2^20)
       uint32_t acc8[NB8];
 #pragma unroll
       for (int b = 0; b < NB8; ++b) acc8[b] = 0;
-      // (no guards on s or on the byte count: the words past s and the table
-      // bytes past each M/m_t are zero, and a uniform branch per dp4a would
-      // cost more issue slots than the zero products)
+      // (no guards on s: the words past s and the table bytes past each
+      // M/m_t are zero, and a uniform branch per dp4a would cost more issue
+      // slots than the zero products)
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        uint32_t wg = wv[4 * g];
-        // (select this output's word without dynamic register indexing)
-        wg = (v == 1) ? wv[4 * g + 1] : wg;
-        wg = (v == 2) ? wv[4 * g + 2] : wg;
-        wg = (v == 3) ? wv[4 * g + 3] : wg;
+      for (int g = 0; g < NG; ++g)
 #pragma unroll
-        for (int b = 0; b < NB8; ++b) acc8[b] = __dp4a(wg, cc.L4[g][b], acc8[b]);
-      }
+        for (int b = 0; b < NBC; ++b) acc8[b] = __dp4a(wsel[g], cc.L4[g][b], acc8[b]);
       // 16-bit limb sums (each below 2^29) as the finishing step expects
       uint32_t acc[NL16];
 #pragma unroll
       for (int l = 0; l < NL16; ++l) acc[l] = acc8[2 * l] + (acc8[2 * l + 1] << 8);
       C[j * ldc + i] = crt_finish<NL16>(acc, cc, ai + beta[j], Xout ? Xout + (j * p_total + i) * 3 : nullptr);
+    };
+    if constexpr (NL16 <= 8) {
+      // unrolled: the four outputs' words are compile-time indices (at 10
+      // limbs the unrolled loop took 171 registers and ran slower)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (jg * 4 + v >= r) break;
+        uint32_t wsel[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) wsel[g] = wv[4 * g + v];
+        one_output(v, wsel);
+      }
+    } else {
+#pragma unroll 1
+      for (int v = 0; v < 4; ++v) {
+        if (jg * 4 + v >= r) break;
+        uint32_t wsel[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          // (select this output's word without dynamic register indexing)
+          uint32_t wg = wv[4 * g];
+          wg = (v == 1) ? wv[4 * g + 1] : wg;
+          wg = (v == 2) ? wv[4 * g + 2] : wg;
+          wg = (v == 3) ? wv[4 * g + 3] : wg;
+          wsel[g] = wg;
+        }
+        one_output(v, wsel);
+      }
     }
   }
 }
@@ -267,9 +290,14 @@ cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t col0
   if (gy < 1) gy = 1;
   const dim3 b(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   const int nl = crt_limbs(s);
-  if (nl == 3) crt_kernel<11, 6><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 4) crt_kernel<15, 8><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else crt_kernel<20, 10><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  // exact instances for the common channel counts (fewer groups and byte
+  // limbs), else the limb-count buckets with MAXS - 1 coefficient bytes
+  if (s == 8) crt_kernel<8, 6, 7><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (s == 14) crt_kernel<14, 8, 13><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (s == 18) crt_kernel<18, 10, 17><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 3) crt_kernel<11, 6, 10><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 4) crt_kernel<15, 8, 14><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else crt_kernel<20, 10, 19><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
   count_launches(1);
   return cudaGetLastError();
 }

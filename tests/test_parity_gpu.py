@@ -78,6 +78,9 @@ def test_small_workload_every_stage(oz2):
 @pytest.mark.parametrize("p,q,r,s", [
     (1, 1, 1, 2), (7, 13, 5, 8), (129, 1000, 257, 14), (1000, 129, 7, 18),
     (300, 70, 513, 20), (64, 961, 40, 14), (130, 1921, 260, 16), (257, 64, 1, 3),
+    # the largest channel count of each CRT limb bucket other than 20 (their
+    # M/m_t use every coefficient byte the bucket's kernel reads)
+    (150, 333, 90, 15), (77, 250, 130, 11),
 ])
 def test_ragged_shapes(oz2, p, q, r, s, mode):
     A, B = make_matrices(p, q, r, 1.0, p * 1000 + q + r + s)
