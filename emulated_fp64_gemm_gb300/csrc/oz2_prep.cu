@@ -303,6 +303,83 @@ __global__ void bound_quant_cols_kernel(const double* __restrict__ B, int64_t q,
   *reinterpret_cast<uint4*>(Bbar + j * qp + l0) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Accu mode, B side in one read of B (q <= 8192): one block per column; thread
+// t holds the column's elements [2048 c + 8 t, +8) in registers, so the column
+// maximum, v_j and the quantised row of Bbar (fp16, zero padded to qp) all come
+// from one read.  Results are identical to amax_cols + bound_quant_cols (an
+// exact integer maximum; the elements past q are zeros, which quantise to 0).
+template <int NCH>
+__global__ void __launch_bounds__(256, 2) fused_cols_bound_kernel(const double* __restrict__ B, int64_t q,
+                                                               int64_t ldb, int64_t qp,
+                                                               uint64_t* __restrict__ amax,
+                                                               int32_t* __restrict__ v_out,
+                                                               uint16_t* __restrict__ Bbar) {
+  __shared__ uint64_t red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t j = blockIdx.x;
+  const double* col = B + j * ldb;
+  const bool vec = (reinterpret_cast<uintptr_t>(col) & 15) == 0;
+  double x[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = c * 2048ll + tid * 8ll;
+    if (vec && l0 + 8 <= q) {
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        const double2 w = __ldg(reinterpret_cast<const double2*>(col + l0 + k));
+        x[c][k] = w.x;
+        x[c][k + 1] = w.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[c][k] = (l0 + k < q) ? __ldg(col + l0 + k) : 0.0;
+    }
+  }
+  uint64_t m = 0;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x[c][k])) & ~(1ull << 63);
+      m = b > m ? b : m;
+    }
+  for (int o = 16; o; o >>= 1) {
+    const uint64_t y = __shfl_xor_sync(0xffffffffu, m, o);
+    m = y > m ? y : m;
+  }
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
+  const int v = quant_exp(m);
+  if (tid == 0) {
+    amax[j] = m;
+    v_out[j] = v;
+  }
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int64_t l0 = c * 2048ll + tid * 8ll;
+    if (l0 < qp) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        uint32_t cq[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const Dec d = decode(x[c][k + h]);
+          cq[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
+        }
+        // fp16 of an integer below 1024: bits 0x6400 + c encode 1024 + c; subtract 1024
+        const uint32_t word = (cq[1] << 16 | cq[0]) + 0x64006400u;
+        __half2 hv = *reinterpret_cast<const __half2*>(&word);
+        hv = __hsub2(hv, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+        w[k >> 1] = *reinterpret_cast<uint32_t*>(&hv);
+      }
+      *reinterpret_cast<uint4*>(Bbar + j * qp + l0) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // accu exponents from the max keys of the bound GEMM.  A key encodes the
 // dyadic value w 2^-x (w < 2^31) as ((floor(log2) + 4096) << 32) | mantissa
 // normalised to 32 bits; 0 encodes zero.  The row value is
@@ -820,12 +897,23 @@ cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, 
   const int splitB = cols_split(a.q, cb, sms);
   const int64_t segB = (a.q + splitB - 1) / splitB;
   amax_rows_kernel<<<dim3(static_cast<unsigned>(rb), splitA), 256, 0, st>>>(a.A, a.p, a.q, a.lda, cpbA, amaxA);
-  amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
+  // B: one read (column in registers) up to q = 8192, else maximum then quantisation
+  const bool fused_b = cols_fused_fast_supported(a.q) && a.r <= 0x7FFFFFFF;
+  if (fused_b) {
+    const dim3 g(static_cast<unsigned>(a.r));
+    const int nch = static_cast<int>((qp + 2047) / 2048);
+    if (nch <= 1) fused_cols_bound_kernel<1><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
+    else if (nch <= 2) fused_cols_bound_kernel<2><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
+    else fused_cols_bound_kernel<4><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
+  } else {
+    amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
+  }
   bound_quant_rows_kernel<<<dim3(static_cast<unsigned>((a.p + 31) / 32), static_cast<unsigned>(qp / 64)), 256, 0, st>>>(
       a.A, a.p, a.q, a.lda, qp, amaxA, u, Abar);
-  bound_quant_cols_kernel<<<dim3(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256)), 256, 0, st>>>(
-      a.B, a.q, a.r, a.ldb, qp, amaxB, v, Bbar);
-  count_launches(4);
+  if (!fused_b)
+    bound_quant_cols_kernel<<<dim3(static_cast<unsigned>((a.r + 7) / 8), static_cast<unsigned>((qp + 255) / 256)), 256, 0, st>>>(
+        a.B, a.q, a.r, a.ldb, qp, amaxB, v, Bbar);
+  count_launches(fused_b ? 3 : 4);
   return cudaGetLastError();
 }
 
