@@ -144,7 +144,10 @@ oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r,
  * Host-memory variant: A, B and C are HOST pointers (pinned memory gives the
  * fastest copies).  The library copies A and B into a device staging area of
  * its workspace, runs ozaki2_dgemm on `stream`, copies C back, and
- * synchronises `stream` before returning.
+ * synchronises `stream` before returning.  With the overlapped schedule the
+ * copies are part of it: A's row blocks and B's column parts go up on a
+ * library-owned stream in the order the kernels consume them, and each part
+ * of C comes back as soon as its CRT has finished.
  */
 oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
                              const double* A, int64_t lda,
@@ -157,11 +160,11 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
  * max_calls ozaki2_dgemm calls records CUDA events at its stage boundaries
  * without synchronising.  ozaki2_dgemm overlaps stages (row blocks: the
  * statistics and residues of block b+1 and the CRT of block b run on a second
- * stream while the GEMMs of block b run on `stream`), so here stage 0 covers
- * the statistics of A's first row block (with all of B's side running beside
- * it on the second stream), stage 2 is the residue time before the first GEMM
- * starts, stage 3 the span of all GEMM launches on
- * `stream`, and stage 4 the CRT time after the last GEMM; stages 0, 1 and 5
+ * stream while the GEMMs of block b run on the library's GEMM stream), so
+ * here stage 0 covers the statistics of A's first row block (with all of B's
+ * side running beside it on the second stream), stage 2 is the residue time
+ * before the first GEMM starts, stage 3 the span of all GEMM launches, and
+ * stage 4 the CRT time after the last GEMM; stages 0, 1 and 5
  * are as for ozaki2_dgemm_stages, which runs the stages one after another.
  * ozaki2_profile_end synchronises those events, writes the per-stage
  * milliseconds summed over the recorded calls to stage_ms_sum[0..5] and the
