@@ -385,3 +385,31 @@ def test_host_entry_point_overlapped_blocks(oz2):
     assert np.all(big.t()[2500:].numpy() == 3.0)
     dev = oz2.dgemm(_dev(A), _dev(B), 14, "fast").cpu().numpy()
     np.testing.assert_array_equal(hC.numpy(), dev)
+
+
+@pytest.mark.parametrize("p,q,r,mode", [(1024, 1024, 1024, "fast"), (2500, 5600, 2500, "fast"),
+                                        (2500, 900, 2000, "accu")])
+def test_cuda_graph_capture_replays_the_call(oz2, p, q, r, mode):
+    """One ozaki2_dgemm call captured into a CUDA graph on a stream whose
+    workspace exists already (a first call grows it; capture allocates
+    nothing).  The overlapped schedule forks onto the library's second and
+    GEMM streams through events, which the capture follows; replays must give
+    the direct call's C bit for bit."""
+    A, B = make_matrices(p, q, r, 0.5, 31)
+    dA, dB = _dev(A), _dev(B)
+    ref = oz2.dgemm(dA, dB, 14, mode).cpu().numpy()
+    st = torch.cuda.Stream()
+    C = torch.full((r, p), float("nan"), dtype=torch.float64, device="cuda").t()
+    with torch.cuda.stream(st):
+        oz2.dgemm(dA, dB, 14, mode, out=C)  # sizes this stream's workspace, creates its streams
+    st.synchronize()
+    C.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        oz2.dgemm(dA, dB, 14, mode, out=C)
+    for _ in range(2):
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(C.cpu().numpy(), ref)
+    assert oz2.last_error() == 0
