@@ -581,7 +581,7 @@ struct Cfg2 {
   static constexpr int B_BYTES = (BN2 / 2) * BK * 2;         // this CTA's half of the tile's rows of B^T
   static constexpr int STAGES = (BN2 == 256) ? 7 : 9;
   static constexpr int STAGE_TX = 2 * (A_BYTES + B_BYTES);   // bytes landing per stage across the pair
-  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;  // 230,656 / 222,464 bytes
+  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;  // 230,656 bytes for BN2 = 256 (the one in use)
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
