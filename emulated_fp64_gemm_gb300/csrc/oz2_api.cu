@@ -322,6 +322,30 @@ oz2_status workspace_sync_objects(Workspace& w) {
   return ok ? OZ2_OK : OZ2_ERR_CUDA;
 }
 
+// Streams and events of a workspace (the device's work on them must be finished).
+void destroy_sync_objects(Workspace& w) {
+  if (!w.aux) return;
+  auto ev = [](cudaEvent_t& e) {
+    if (e) cudaEventDestroy(e);
+    e = nullptr;
+  };
+  ev(w.ev_ready);
+  ev(w.ev_done);
+  ev(w.ev_start);
+  ev(w.ev_bready);
+  ev(w.ev_io);
+  ev(w.ev_gemm_go);
+  for (auto& e : w.ev_res) ev(e);
+  for (auto& e : w.ev_upA) ev(e);
+  for (auto& e : w.ev_upB) ev(e);
+  for (auto& e : w.ev_bpart) ev(e);
+  for (auto& e : w.ev_gemm) ev(e);
+  for (cudaStream_t* sp : {&w.aux, &w.up, &w.gemm}) {
+    if (*sp) cudaStreamDestroy(*sp);
+    *sp = nullptr;
+  }
+}
+
 oz2_status get_workspace(cudaStream_t st, size_t bytes, uint8_t** base, Workspace** wout = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ2_ERR_CUDA;
@@ -907,11 +931,10 @@ void ozaki2_workspace_release(void) {
   int cur = 0;
   cudaGetDevice(&cur);
   for (auto& kv : g_ws) {
-    if (kv.second.base) {
-      cudaSetDevice(kv.first.first);
-      cudaDeviceSynchronize();
-      cudaFree(kv.second.base);
-    }
+    cudaSetDevice(kv.first.first);
+    cudaDeviceSynchronize();
+    if (kv.second.base) cudaFree(kv.second.base);
+    destroy_sync_objects(kv.second);  // the second, upload and GEMM streams and their events
   }
   g_ws.clear();
   cudaSetDevice(cur);
@@ -921,7 +944,7 @@ const char* ozaki2_status_string(oz2_status status) {
   switch (status) {
     case OZ2_OK: return "ok";
     case OZ2_ERR_INVALID_ARG: return "invalid argument";
-    case OZ2_ERR_Q_TOO_LARGE: return "inner dimension q >= 131072";
+    case OZ2_ERR_Q_TOO_LARGE: return "inner dimension q at or above its mode's limit";
     case OZ2_ERR_NO_MEMORY: return "workspace allocation failed";
     case OZ2_ERR_CUDA: return "CUDA error";
     case OZ2_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";

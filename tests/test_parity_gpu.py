@@ -413,3 +413,19 @@ def test_cuda_graph_capture_replays_the_call(oz2, p, q, r, mode):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(C.cpu().numpy(), ref)
     assert oz2.last_error() == 0
+
+
+def test_workspace_release_and_recreate(oz2):
+    """ozaki2_workspace_release frees the workspaces and destroys the library's
+    streams and events; the next call builds them again and gives the same C."""
+    A, B = make_matrices(2500, 900, 2000, 0.5, 41)  # accu: above the one-block size, overlapped
+    dA, dB = _dev(A), _dev(B)
+    C0 = oz2.dgemm(dA, dB, 14, "accu").cpu().numpy()
+    oz2.workspace_release()
+    C1 = oz2.dgemm(dA, dB, 14, "accu").cpu().numpy()
+    np.testing.assert_array_equal(C1, C0)
+    oz2.workspace_release()
+    C2 = oz2.dgemm(dA, dB, 14, "fast").cpu().numpy()
+    ref = oracle.oracle_entries(A, B, 14, "fast", np.arange(0, 2500, 97), np.arange(0, 2000, 79)[:26])
+    assert ulp_distance(C2[np.arange(0, 2500, 97), np.arange(0, 2000, 79)[:26]], ref["C"]) <= ULP_TOL
+    assert oz2.last_error() == 0
