@@ -446,7 +446,8 @@ def run_ours(args, rank, world, local):
         hA = torch.from_numpy(A).pin_memory()
         hB = torch.from_numpy(B).pin_memory()
         hC = torch.empty((w.r, w.p), dtype=torch.float64).pin_memory().t()
-        oz2.dgemm_host(hA, hB, w.s, w.mode, out=hC)  # sizes the staging workspace
+        for _ in range(max(1, args.warmup)):  # the first call sizes the staging workspace
+            oz2.dgemm_host(hA, hB, w.s, w.mode, out=hC)
         barrier()
         t0 = time.perf_counter()
         per_call = []
