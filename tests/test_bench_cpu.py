@@ -23,6 +23,20 @@ def test_result_line_has_the_contract_keys():
     assert other["vs_baseline"] is None
 
 
+def test_metric_names_the_workload_and_traffic_is_tied_to_the_profiled_source():
+    # the headline keeps the contract's metric string; other workloads name their shape and mode
+    assert bench.metric_name(bench.HEADLINE) == bench.METRIC
+    other = bench.metric_name("n4096_s14_accu")
+    assert "p=4096 q=4096 r=4096 s=14 accu" in other and other != bench.METRIC
+    line = bench.result_line(value=1.0, n_gpus=1, steps=1, warmup=3, ms_per_step=1.0,
+                             workload="n4096_s14_accu", extra={})
+    assert line["metric"] == other
+    # the committed GEMM profile matches the current kernel source, so its traffic is reported
+    assert bench.GEMM_PROFILE_WORKLOAD == bench.HEADLINE
+    t = bench.gemm_traffic_per_unit()
+    assert t is not None and t > 0
+
+
 def test_clock_sampler_without_nvidia_smi_returns_none():
     c = bench.ClockSampler(0)
     c.start()
