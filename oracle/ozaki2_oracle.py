@@ -20,7 +20,7 @@ Sources (web pages; cited by title and section):
        condition, §1.4 range bits, §2 Eq. (18).
 
 The pages leave several rules open; the readings taken here are numbered
-R1..R10 in the docstrings below and collected in the design notes.
+R1..R14 in the docstrings below and collected in the design notes.
 
 Parity pins (tests/test_oracle_pins.py) tie every function here to something
 other than itself: brute force on tiny inputs (X == A'B' with Python big
