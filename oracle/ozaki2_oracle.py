@@ -36,8 +36,10 @@ from fractions import Fraction
 import numpy as np
 
 # Fractional bits kept per element in the fast-mode sum-of-squares statistic
-# (reading R5).  Each rounded-up term is <= 2**(2F), so for q < 2**24 the sum
-# of squares is < 2**64 and fits a 64-bit integer (FAST_Q_LIMIT).
+# (reading R5).  Each rounded-up term is <= 2**F and its square <= 2**(2F),
+# so for q < 2**24 the sum of squares is < 2**64 and fits an unsigned 64-bit
+# integer (FAST_Q_LIMIT); it is summed in uint64, since from q = 2**23 on it
+# can pass 2**63.
 F_FAST = 20
 # Largest magnitude of an upward-quantised bound entry: signed INT8 (reading R6).
 BOUND_QMAX = 127
@@ -128,6 +130,8 @@ def ceil_scaled(mant: np.ndarray, E: np.ndarray, k) -> np.ndarray:
 
 def max_pow4_exponent(U: Fraction, L: int) -> int:
     """max { a in Z : 4**a * U <= L }, and 0 when U == 0 (reading R4)."""
+    if U < 0:
+        raise ValueError("a bound on a sum of squares or of |A||B| cannot be negative")
     if U == 0:
         return 0
     # start near the answer from bit lengths, then step to the exact maximum
@@ -164,7 +168,12 @@ def fast_exponents(X: np.ndarray, axis: int, L: int) -> np.ndarray:
     e = floor_log2_plus1(amax)
     e_b = np.expand_dims(e, axis)
     terms = ceil_scaled(mant, E, F_FAST - e_b)
-    S = np.sum(terms * terms, axis=axis)
+    # each term is <= 2**F, its square <= 2**(2F) = 2**40, so a sum of q < 2**24
+    # squares is < 2**64: exact in uint64 (int64 would wrap from q >= 2**23)
+    if X.shape[axis] >= FAST_Q_LIMIT:
+        raise ValueError("q >= 2**24: the sum of squares may leave 64 bits")
+    sq = (terms * terms).astype(np.uint64)
+    S = np.sum(sq, axis=axis, dtype=np.uint64)
     out = np.zeros(S.shape, dtype=np.int64)
     for i in range(S.shape[0]):
         Si = int(S[i])

@@ -294,6 +294,102 @@ def test_fast_statistic_sandwich_and_near_maximality():
         assert Fraction(4) ** (a + 1) * hi > L  # no larger exponent is provably safe
 
 
+def _max_pow4_brute(U: Fraction, L: int) -> int:
+    """max { a : 4**a U <= L } by stepping from a = 0 (U > 0), independent of the oracle."""
+    a = 0
+    if Fraction(4) ** a * U <= L:
+        while Fraction(4) ** (a + 1) * U <= L:
+            a += 1
+    else:
+        while Fraction(4) ** a * U > L:
+            a -= 1
+    return a
+
+
+@pytest.mark.parametrize("q", [1 << 23, (1 << 23) + 1])
+def test_fast_statistic_past_two_to_the_63(q):
+    """[P] §5.1 (sum of squares rounded up), reading R5 at the top of its range.
+
+    Every entry is 1 - 2**-53, the largest double below 1: e = 0 and every
+    rounded-up term is ceil((1 - 2**-53) 2**20) = 2**20, so S = q 2**40 >= 2**63
+    (a signed 64-bit sum wraps here) and U = S 4**-20 = q exactly."""
+    x = 1.0 - 2.0**-53
+    row = np.full((1, q), x)
+    for s in (8, 14, 20):
+        L = oz.modulus_constants(oz.greedy_moduli(s))["L"]
+        got = int(oz.fast_exponents(row, axis=1, L=L)[0])
+        assert got == _max_pow4_brute(Fraction(q), L)
+        # sound against the exact squared norm, and the next exponent is not
+        n2 = q * Fraction(x) ** 2
+        assert Fraction(4) ** got * n2 <= L < Fraction(4) ** (got + 1) * Fraction(q)
+    col = np.full((q, 1), x)
+    L = oz.modulus_constants(oz.greedy_moduli(14))["L"]
+    assert int(oz.fast_exponents(col, axis=0, L=L)[0]) == _max_pow4_brute(Fraction(q), L)
+
+
+def _max_scaled_brute(W, w_exp, axis):
+    """max along axis of Fraction(W) 2**-w_exp, by brute force over exact values."""
+    W = np.asarray(W)
+    we = np.broadcast_to(w_exp, W.shape)
+    n = W.shape[1 - axis]
+    out = []
+    for k in range(n):
+        vals = [Fraction(int(W[l, k] if axis == 0 else W[k, l])) *
+                Fraction(2) ** (-int(we[l, k] if axis == 0 else we[k, l])) for l in range(W.shape[axis])]
+        out.append(max(vals))
+    return out
+
+
+def test_max_scaled_exact_fallback_and_fast_path():
+    """The accu maxima max_j Wbar_ij 2**-v_j (rows) and max_i Wbar_ij 2**-u_i
+    (columns) against brute force over exact Fractions: once on ordinary
+    values (float path) and once where the scaled values are subnormal or
+    would not round-trip in float64 (exact Fraction path)."""
+    rng = np.random.default_rng(12)
+    W = rng.integers(0, 2**31, size=(6, 5)).astype(np.int64)
+    u = rng.integers(-40, 40, size=6)
+    v = rng.integers(-40, 40, size=5)
+    cases = [(W, u, v)]
+    # subnormal-range exponents: 2**-1070 Wbar is subnormal; 2**-1060 Wbar would round
+    W2 = W.copy()
+    W2[2, :] = [3, 2**30 + 1, 7, 0, 2**31 - 1]
+    u2 = u.copy()
+    u2[2] = 1070
+    v2 = v.copy()
+    v2[3] = 1060
+    cases.append((W2, u2, v2))
+    # two candidates that float64 cannot tell apart: (2**30 + 1) 2**-1080 rounds to 2**-1050
+    W3 = np.zeros((3, 2), dtype=np.int64)
+    W3[0, 0], W3[1, 0], W3[2, 1] = 2**30, 2**30 + 1, 5
+    cases.append((W3, np.array([1080, 1080, 0]), np.array([1080, 1080])))
+    for Wc, uc, vc in cases:
+        for axis, wexp in ((1, vc[None, :]), (0, uc[:, None])):
+            idx = oz._max_scaled(Wc, wexp, axis)
+            want = _max_scaled_brute(Wc, wexp, axis)
+            we = np.broadcast_to(wexp, Wc.shape)
+            for k, l in enumerate(idx):
+                i, j = (k, int(l)) if axis == 1 else (int(l), k)
+                assert Fraction(int(Wc[i, j])) * Fraction(2) ** (-int(we[i, j])) == want[k]
+
+
+def test_accu_exponents_subnormal_row_and_huge_column():
+    """accu mode with a row of |a| ~ 1e-310 (u_i ~ 1030, so its scaled bound
+    products are subnormal) and a column of B near 1e300 (v_j ~ -990): alpha
+    and beta against exact brute-force maxima of Wbar_ij 2**-(u_i + v_j)."""
+    A, B = make_matrices(5, 12, 4, 1.0, 44)
+    A[1, :] *= 1e-310
+    B[:, 2] *= 1e300
+    L = oz.modulus_constants(oz.greedy_moduli(14))["L"]
+    al, be, Abar, Bbar, u, v, W = oz.accu_exponents(A, B, L)
+    assert u[1] > 1000 and v[2] < -900
+    for i in range(5):
+        Ui = max(Fraction(int(W[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) for j in range(4))
+        assert int(al[i]) == (_max_pow4_brute(Ui, L) if Ui else 0)
+    for j in range(4):
+        Vj = max(Fraction(int(W[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) for i in range(5))
+        assert int(be[j]) == (_max_pow4_brute(Vj, L) if Vj else 0)
+
+
 def test_accu_bound_dominates_abs_product():
     A, B = make_matrices(4, 10, 5, 2.0, 31)
     c = oz.modulus_constants(oz.greedy_moduli(14))
@@ -381,7 +477,7 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     def fails(fn):
         try:
             fn()
-        except AssertionError:
+        except (AssertionError, ValueError):
             return True
         return False
 
@@ -422,3 +518,26 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     assert fails(run)
     monkeypatch.setattr(oz, "fast_exponents", orig_fast)
     assert not fails(run)
+
+    # the fast statistic summed in signed 64 bits wraps at q = 2**23
+    class Int64Sum:
+        def __getattr__(self, name):
+            return getattr(np, name)
+
+        @staticmethod
+        def sum(a, axis=None, dtype=None):
+            return np.sum(np.asarray(a).astype(np.int64), axis=axis, dtype=np.int64)
+
+    big = lambda: test_fast_statistic_past_two_to_the_63(1 << 23)
+    assert not fails(big)
+    monkeypatch.setattr(oz, "np", Int64Sum())
+    assert fails(big)
+    monkeypatch.setattr(oz, "np", np)
+
+    # the accu maxima taken in float64 alone (no exact fallback)
+    orig_ms = oz._max_scaled
+    monkeypatch.setattr(oz, "_max_scaled", lambda W, we, axis: np.argmax(
+        np.ldexp(np.asarray(W, dtype=np.float64), -we), axis=axis))
+    assert fails(test_max_scaled_exact_fallback_and_fast_path)
+    monkeypatch.setattr(oz, "_max_scaled", orig_ms)
+    assert not fails(test_max_scaled_exact_fallback_and_fast_path)
