@@ -6,8 +6,9 @@ n = 8192, s = 14, fast workload (the study's headline configuration), with
 the per-stage milliseconds of the same calls.  One step = one full call
 (scaling, residues, the s modular GEMMs, CRT) on inputs already in HBM.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--s S] [--mode M]
+    python bench.py --impl reference ...   # the native CPU oracle on a bounded sample
+    python bench.py --sweep                # ms per call and per stage over s, n and mode
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the method has no exchange step on one problem; weak scaling); the timed
@@ -17,6 +18,7 @@ One JSON line is printed by rank 0.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -38,11 +40,11 @@ METRIC = "effective FP64 TFLOPS (2pqr/time), Ozaki-II n=8192 s=14 fast; per-stag
 GEMM_PROFILE_WORKLOAD = "n8192_s14_fast"
 
 
-def metric_name(workload: str) -> str:
+def metric_name(workload) -> str:
     """The headline metric string; other workloads name their own shape and mode."""
-    if workload == HEADLINE:
+    w = WORKLOADS[workload] if isinstance(workload, str) else workload
+    if w == WORKLOADS[HEADLINE]:
         return METRIC
-    w = WORKLOADS[workload]
     return (f"effective FP64 TFLOPS (2pqr/time), Ozaki-II p={w.p} q={w.q} r={w.r} s={w.s} {w.mode}; "
             "per-stage ms")
 UNIT = "TFLOP/s"
@@ -53,7 +55,19 @@ GEMM_PROFILE = os.path.join(ROOT, "profiles", "oz2_gemm_kernel_n8192_s14_fast.md
 # the GEMM kernel's source files, hashed in this order against the summary's source_sha256
 GEMM_SOURCES = [os.path.join(ROOT, "emulated_fp64_gemm_gb300", "csrc", f)
                 for f in ("oz2_gemm.cu", "oz2_tcgen05.cuh")]
-CPU_SAMPLE = 512  # rows of A and columns of B in the oracle's bounded sample
+# rows of A and columns of B in each step of the reference arm's bounded sample
+REF_SAMPLE = 2048
+# sampled outputs of the accuracy report
+ACCURACY_SAMPLES = 4096
+# the native oracle's exact integer products (the C loops or an exact float64 BLAS product)
+ORACLE_PRODUCTS = "blas"
+# bytes per stored residue: the planes are fp16 (integer residues, exact in fp16)
+PLANE_BYTES = 2
+# the library's one-read kernels: A's statistics and residues together for q <= 2048,
+# B's for q <= 8192 (fast mode); a stage's algorithmic bytes follow what it runs
+ROWS_FUSED_MAX_Q, COLS_FUSED_MAX_Q = 2048, 8192
+SWEEP_S = (2, 4, 6, 8, 10, 12, 14, 16, 18, 20)
+SWEEP_N = (1024, 2048, 8192)
 
 
 def parse_args(argv=None):
@@ -63,6 +77,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--s", type=int, default=None, help="number of moduli (overrides the workload's)")
+    ap.add_argument("--mode", choices=["fast", "accu"], default=None, help="bound mode (overrides the workload's)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every s in %s at n in %s, fast and accu (one JSON line each)" % (SWEEP_S, SWEEP_N))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true",
@@ -240,11 +258,22 @@ def aggregate_max(x: float) -> float:
     return float(t.item())
 
 
+def resolve_workload(args):
+    """The named workload, with --s / --mode applied (a new name when they change it)."""
+    w = WORKLOADS[args.workload]
+    s = args.s if args.s is not None else w.s
+    mode = args.mode if args.mode is not None else w.mode
+    if (s, mode) == (w.s, w.mode):
+        return w
+    base = w.name.rsplit("_s", 1)[0]
+    return dataclasses.replace(w, name=f"{base}_s{s}_{mode}", s=s, mode=mode)
+
+
 def result_line(*, value, n_gpus, steps, warmup, ms_per_step, workload, extra):
-    w = WORKLOADS[workload]
-    base = PAGES_BASELINE.get(workload)
+    w = WORKLOADS[workload] if isinstance(workload, str) else workload
+    base = PAGES_BASELINE.get(w.name) if w == WORKLOADS.get(w.name) else None
     out = {
-        "metric": metric_name(workload),
+        "metric": metric_name(w),
         "value": value,
         "unit": UNIT,
         "n_gpus": n_gpus,
@@ -257,7 +286,7 @@ def result_line(*, value, n_gpus, steps, warmup, ms_per_step, workload, extra):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": workload, "p": w.p, "q": w.q, "r": w.r, "s": w.s, "mode": w.mode,
+            "workload": w.name, "p": w.p, "q": w.q, "r": w.r, "s": w.s, "mode": w.mode,
             "phi": w.phi, "seed": w.seed, "io_dtype": "f64",
             "tensor_path": "tcgen05.mma kind::f16 on integer residues, fp32 TMEM accumulation",
             "l2": "inputs larger than L2 (A+B = %.2f GB vs 129 MB)" % (8e-9 * (w.p * w.q + w.q * w.r)),
@@ -269,29 +298,114 @@ def result_line(*, value, n_gpus, steps, warmup, ms_per_step, workload, extra):
     return out
 
 
+# ----------------------------------------------------------------------------- stage rooflines
+def stage_work(w):
+    """Algorithmic work of each stage of the stage-timed (sequential) pass.
+
+    HBM stages count the bytes the method must move: every input double read
+    once (8 B), every residue written once (PLANE_BYTES per residue, s per
+    input element), every CRT coefficient byte read once and every output
+    double written once ((s + 8) B per output).  In fast mode the one-read
+    kernels make A's (q <= 2048) and B's (q <= 8192) residue planes in the
+    statistics stage, so those planes count there.  Accu's quantisation
+    stage reads A and B and writes the fp16 bound planes.  The GEMM stages
+    count 2pqr (bound) and 2 s pqr (modular) flops."""
+    pq, qr, pr = w.p * w.q, w.q * w.r, w.p * w.r
+    res_a = (8 + PLANE_BYTES * w.s) * pq
+    res_b = (8 + PLANE_BYTES * w.s) * qr
+    if w.mode == "fast":
+        fused_a, fused_b = w.q <= ROWS_FUSED_MAX_Q, w.q <= COLS_FUSED_MAX_Q
+        scale = (res_a if fused_a else 8 * pq) + (res_b if fused_b else 8 * qr)
+        residues = (0 if fused_a else res_a) + (0 if fused_b else res_b)
+        bound_flops = 0.0
+    else:
+        scale = (8 + PLANE_BYTES) * (pq + qr)
+        residues = res_a + res_b
+        bound_flops = 2.0 * pq * w.r
+    return {"scale": ("hbm", float(scale)), "bound_gemm": ("tensor", bound_flops),
+            "residues": ("hbm", float(residues)), "gemm_mod": ("tensor", 2.0 * w.s * pq * w.r),
+            "crt": ("hbm", float((w.s + 8) * pr))}
+
+
+def stage_roofline(w, stage_ms, hbm_gbs, tensor_tflops):
+    """Each stage's achieved rate (its algorithmic work / its time) against its
+    roofline; 'suspect' marks a fraction above 1.2, which would mean the
+    timing does not cover the work."""
+    out = {}
+    for name, (bound, work) in stage_work(w).items():
+        ms = stage_ms.get(name, 0.0)
+        if work <= 0 or ms <= 0:
+            continue
+        if bound == "hbm":
+            rate = work / (ms * 1e-3) / 1e9
+            e = {"bound": "hbm", "ms": ms, "bytes": work, "GBps": rate, "peak_GBps": hbm_gbs,
+                 "frac": rate / hbm_gbs}
+        else:
+            rate = work / (ms * 1e-3) / 1e12
+            e = {"bound": "tensor", "ms": ms, "flops": work, "TFLOPs": rate, "peak_TFLOPs": tensor_tflops,
+                 "frac": rate / tensor_tflops}
+        e["suspect"] = e["frac"] > 1.2
+        out[name] = e
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU oracle
+def oracle_full(A, B, w):
+    """The native oracle on the whole problem, every stage, on all host cores: (C, seconds)."""
+    from oracle import native
+
+    t0 = time.perf_counter()
+    C = native.dgemm(A, B, w.s, w.mode, want=("C",), products=ORACLE_PRODUCTS)["C"]
+    return C, time.perf_counter() - t0
+
+
 def oracle_sample(A, B, w, n):
-    """Time the oracle on the leading n x q x n block of the workload."""
-    from oracle import ozaki2_oracle as oracle
+    """Time the native oracle on the leading n x q x n block: (TFLOP/s, seconds)."""
+    from oracle import native
 
     a = A[:n, :]
     b = B[:, :n]
     t0 = time.perf_counter()
-    oracle.oracle_dgemm(a, b, w.s, w.mode)
+    native.dgemm(a, b, w.s, w.mode, want=("C",), products=ORACLE_PRODUCTS)
     dt = time.perf_counter() - t0
-    return 2.0 * n * w.q * n / dt / 1e12, dt
+    return 2.0 * a.shape[0] * w.q * b.shape[1] / dt / 1e12, dt
 
 
 def cpu_cores():
-    return os.cpu_count() or 1
+    from oracle import native
+
+    return native.threads()
+
+
+def accuracy_report(A, B, w, C_gpu, C_oracle=None):
+    """Normwise and componentwise errors of the GPU's and the oracle's C against
+    the exact product, on ACCURACY_SAMPLES seeded sampled outputs."""
+    import numpy as np
+
+    from oracle import native
+
+    rng = np.random.default_rng(4242)
+    n = min(ACCURACY_SAMPLES, w.p * w.r)
+    ii = rng.integers(0, w.p, n)
+    jj = rng.integers(0, w.r, n)
+    if C_oracle is not None:
+        co = np.asarray(C_oracle)[ii, jj]
+    else:
+        al, be = native.exponents(A, B, w.s, w.mode)
+        co = native.entries(A, B, w.s, al, be, ii, jj)["C"]
+    rep = native.accuracy_at(A, B, ii, jj, {"gpu": np.asarray(C_gpu)[ii, jj], "oracle": co})
+    rep["not_worse_than_oracle"] = bool(rep["gpu"]["normwise"] <= rep["oracle"]["normwise"] and
+                                        rep["gpu"]["componentwise"] <= rep["oracle"]["componentwise"])
+    rep["against"] = "exact products (fixed-point accumulator of the native oracle), sampled outputs"
+    return rep
 
 
 def run_reference(args, rank):
     if rank != 0:
         return 0
-    w = WORKLOADS[args.workload]
+    w = resolve_workload(args)
     A, B = make_workload(w)
-    n = 256
+    n = min(REF_SAMPLE, w.p, w.r)
     for _ in range(args.warmup):
         oracle_sample(A, B, w, n)
     times = []
@@ -299,9 +413,10 @@ def run_reference(args, rank):
         times.append(oracle_sample(A, B, w, n)[1])
     total = sum(times)
     value = args.steps * 2.0 * n * w.q * n / total / 1e12
-    sample = f"leading {n}x{w.q}x{n} block of the {args.workload} workload per step"
+    sample = (f"leading {n}x{w.q}x{n} block of the {w.name} workload per step; the native oracle "
+              f"(every stage; exact products as a float64 BLAS product) on {cpu_cores()} host threads")
     line = result_line(value=value, n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
-                       ms_per_step=1e3 * total / args.steps, workload=args.workload, extra={
+                       ms_per_step=1e3 * total / args.steps, workload=w, extra={
                            "impl": "reference",
                            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(),
                                             "kind": "oracle", "sample": sample},
@@ -315,6 +430,29 @@ def run_reference(args, rank):
 
 
 # ----------------------------------------------------------------------------- our arm
+def time_calls(oz2, torch, dA, dB, C, w, steps, stream):
+    """Device time (ms) of `steps` back-to-back ozaki2_dgemm calls, CUDA events on `stream`."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        oz2.dgemm(dA, dB, w.s, w.mode, out=C)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def sequential_stages(oz2, torch, dA, dB, C, w, reps):
+    """Mean per-stage ms over `reps` calls of the stage-timed entry point, whose
+    stages run one after another (the kernels of each stage alone on the GPU)."""
+    acc = {}
+    for _ in range(reps):
+        _, ms = oz2.dgemm_stages(dA, dB, w.s, w.mode, out=C)
+        for k, v in ms.items():
+            acc[k] = acc.get(k, 0.0) + v
+    return {k: v / reps for k, v in acc.items()}
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -325,7 +463,7 @@ def run_ours(args, rank, world, local):
     import emulated_fp64_gemm_gb300 as oz2
 
     torch.cuda.set_device(local)
-    w = WORKLOADS[args.workload]
+    w = resolve_workload(args)
     A, B = make_workload(w)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
@@ -346,35 +484,25 @@ def run_ours(args, rank, world, local):
             gpu_index = local
     clocks = ClockSampler(gpu_index)
 
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.25)  # let the sampler take its first reading
     n0 = oz2.launch_count()
-    e0.record(stream)
-    for _ in range(args.steps):
-        oz2.dgemm(dA, dB, w.s, w.mode, out=C)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    local_ms = time_calls(oz2, torch, dA, dB, C, w, args.steps, stream)
     launches = oz2.launch_count() - n0
     barrier()
     clk = clocks.stop()
-    local_ms = e0.elapsed_time(e1)
 
-    # the per-stage split comes from a second, instrumented pass of the same
-    # calls (events at the stage boundaries); its own time gives the overhead
-    # of instrumenting, which the clean pass above does not carry
+    # the GEMM span of the same calls comes from a second, instrumented pass
+    # (events at the stage boundaries of the overlapped schedule); its own time
+    # gives the overhead of instrumenting, which the clean pass above does not carry
     oz2.profile_begin(args.steps)
-    e0.record(stream)
-    for _ in range(args.steps):
-        oz2.dgemm(dA, dB, w.s, w.mode, out=C)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    instrumented_ms = time_calls(oz2, torch, dA, dB, C, w, args.steps, stream) / args.steps
     ncalls, stage_sum = oz2.profile_end()
-    instrumented_ms = e0.elapsed_time(e1) / args.steps
     max_ms = aggregate_max(local_ms)
+    # per-stage rooflines: the stage-timed entry point runs the stages one after another
+    seq = sequential_stages(oz2, torch, dA, dB, C, w, reps=3)
     status = oz2.last_error()
     if status != 0:
         raise RuntimeError(f"device-side error word set: {status}")
@@ -391,24 +519,21 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "tensor", "kernel": "oz2_gemm2sm_kernel (CTA-pair tcgen05, mod epilogue)",
                 "unit_of_work": "the GEMM stage of one call (all its GEMM launches)", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": gemm_traffic_per_unit() if args.workload == GEMM_PROFILE_WORKLOAD else None,
+                "traffic": gemm_traffic_per_unit() if w.name == GEMM_PROFILE_WORKLOAD else None,
                 "peak_source": f"{how} bf16 dense burst (f16 kind::f16 runs at the bf16 rate)",
                 "algorithmic": "2*s*p*q*r flops per launch"}
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    e_in = w.p * w.q + w.q * w.r
-    stage_roofline = {
-        "scale_GBps": 2 * 8 * e_in / (stages["scale"] * 1e-3) / 1e9 if stages["scale"] > 0 else None,
-        "residues_GBps": (8 + 2 * w.s) * e_in / (stages["residues"] * 1e-3) / 1e9,
-        "crt_GBps": (w.s + 8) * w.p * w.r / (stages["crt"] * 1e-3) / 1e9,
-        "hbm_peak_GBps": hbm,
-    }
     extra = {"impl": "ours", "roofline": roofline, "stages_ms": stages,
              "stages_note": ("from a second, instrumented pass of the same calls; overlapped schedule: "
                              "residues = residue time before the first GEMM, gemm_mod = span of the GEMM "
                              "launches, crt = CRT time after the last GEMM"),
              "instrumented_ms_per_step": instrumented_ms,
              "instrumenting_overhead": instrumented_ms / ms_per_step - 1.0,
-             "stage_bandwidth": stage_roofline, "gpu_launches": launches}
+             "stage_roofline": {"pass": "ozaki2_dgemm_stages (stages one after another), mean of 3 calls",
+                                "peak_source": f"{how} HBM copy and bf16 dense burst",
+                                "total_ms": seq.get("total"),
+                                "stages": stage_roofline(w, seq, hbm, peak)},
+             "gpu_launches": launches}
     if clk is not None:
         extra["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                            "reasons": clk["reasons"], "samples": clk["samples"]}
@@ -442,6 +567,7 @@ def run_ours(args, rank, world, local):
         del ref, dCe
 
     # end to end through the host-memory entry point: H2D of A and B, D2H of C
+    e_in = w.p * w.q + w.q * w.r
     if not args.no_e2e:
         hA = torch.from_numpy(A).pin_memory()
         hB = torch.from_numpy(B).pin_memory()
@@ -463,26 +589,73 @@ def run_ours(args, rank, world, local):
                         "median_ms_per_call": 1e3 * statistics.median(per_call),
                         "max_ms_per_call": 1e3 * max(per_call)}
         got = hC.numpy()
-        dev_c = C.cpu().numpy()
-        if not np.array_equal(got, dev_c):
+        if not np.array_equal(got, C.cpu().numpy()):
             raise RuntimeError("host entry point disagrees with the device entry point")
+        del hA, hB, hC
 
+    C_gpu = C.cpu().numpy()
+    del dA, dB, C
+    torch.cuda.empty_cache()
+    C_oracle = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt = oracle_sample(A, B, w, CPU_SAMPLE)
-        extra["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                                 "sample": f"leading {CPU_SAMPLE}x{w.q}x{CPU_SAMPLE} block, "
-                                           f"{dt:.1f} s; BLAS products on all cores, the rest on one"}
+        C_oracle, dt = oracle_full(A, B, w)
+        v = w.flops / dt / 1e12
+        extra["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"full problem ({w.p}x{w.q}x{w.r}, s={w.s}, {w.mode}), {dt:.1f} s: the native oracle, "
+                       f"every stage on {cpu_cores()} host threads, exact products as a float64 BLAS product")}
+        # the oracle's C for the whole problem doubles as a full elementwise check of the timed output
+        extra["full_parity"] = {"entries": int(C_gpu.size), "identical": bool(np.array_equal(C_gpu, C_oracle)),
+                                "max_ulp": entry.ulp_distance(C_gpu, C_oracle), "tolerance_ulp": 2}
     if rank == 0:
+        extra["accuracy"] = accuracy_report(A, B, w, C_gpu, C_oracle)
         print(json.dumps(result_line(value=value, n_gpus=world, steps=args.steps,
                                      warmup=args.warmup, ms_per_step=ms_per_step,
-                                     workload=args.workload, extra=extra)), flush=True)
+                                     workload=w, extra=extra)), flush=True)
+    return 0
+
+
+def run_sweep(args):
+    """ms per call (clean pass) and per stage (stage-timed pass) for every s in
+    SWEEP_S at n in SWEEP_N, fast and accu, phi = 0.5, seed 123456: one JSON
+    line per configuration."""
+    import torch
+
+    import __graft_entry__ as entry
+    from workloads import Workload, make_matrices
+
+    entry.build()
+    import emulated_fp64_gemm_gb300 as oz2
+
+    stream = torch.cuda.current_stream()
+    for n in SWEEP_N:
+        A, B = make_matrices(n, n, n, 0.5, 123456)
+        dA = torch.from_numpy(A).cuda()
+        dB = torch.from_numpy(B).cuda()
+        C = torch.empty((n, n), dtype=torch.float64, device="cuda").t()
+        steps = max(3, min(args.steps, 30))
+        for mode in ("fast", "accu"):
+            for s in SWEEP_S:
+                w = Workload(f"n{n}_s{s}_{mode}", n, n, n, s, mode, 0.5, 123456)
+                for _ in range(3):
+                    oz2.dgemm(dA, dB, s, mode, out=C)
+                torch.cuda.synchronize()
+                ms = time_calls(oz2, torch, dA, dB, C, w, steps, stream) / steps
+                seq = sequential_stages(oz2, torch, dA, dB, C, w, reps=3)
+                print(json.dumps({"sweep": True, "n": n, "s": s, "mode": mode, "steps": steps,
+                                  "ms_per_call": ms, "tflops": w.flops / ms / 1e9,
+                                  "sequential_stages_ms": seq}), flush=True)
+        del dA, dB, C
+        torch.cuda.empty_cache()
     return 0
 
 
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_setup()
-    if args.impl == "reference":
+    if args.sweep:
+        rc = run_sweep(args) if rank == 0 else 0
+    elif args.impl == "reference":
         rc = run_reference(args, rank)
     else:
         rc = run_ours(args, rank, world, local)

@@ -6,9 +6,9 @@ PyTorch supplies device memory and streams.  There is no CPU fallback: if
 the library is not built, loading it raises.
 
 Matrices follow the library's column-major convention: a (p, q) tensor with
-strides (1, ld), ld >= p, is passed as is.  Row-major (C-contiguous) operands
-are handled through C^T = B^T A^T, which is the same computation with the
-roles of the row and column scalings exchanged, so the result is identical.
+strides (1, ld), ld >= p, is passed as is.  Any other layout (row-major,
+or a non-unit row stride) is first copied into a column-major tensor on the
+same device, so the library always sees column-major operands.
 """
 from __future__ import annotations
 
@@ -35,6 +35,7 @@ _lib = None
 STATUS = {
     0: "OZ2_OK", 1: "OZ2_ERR_INVALID_ARG", 2: "OZ2_ERR_Q_TOO_LARGE", 3: "OZ2_ERR_NO_MEMORY",
     4: "OZ2_ERR_CUDA", 5: "OZ2_ERR_DEVICE_TIMEOUT", 6: "OZ2_ERR_UNSUPPORTED_DEVICE",
+    7: "OZ2_ERR_SCRATCH_TOO_SMALL",
 }
 
 

@@ -415,7 +415,7 @@ struct HostIO {
 // them, and each finished part of C is copied to io->C as soon as its CRT is
 // done.
 oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
-                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, oz2_mode mode,
                         cudaStream_t st, const Outputs* dbg, cudaEvent_t* ev, uint8_t** ws_out,
                         Layout* lay_out, bool pipelined, const HostIO* io = nullptr) {
   double* hostC = io ? io->C : nullptr;
@@ -771,7 +771,7 @@ using namespace oz2;
 extern "C" {
 
 oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
-                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                        const double* B, int64_t ldb, double* C, int64_t ldc, int s, oz2_mode mode,
                         void* stream) {
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
   if (e != OZ2_OK) return e;
@@ -826,7 +826,7 @@ oz2_status ozaki2_profile_end(float* stage_ms_sum, int* ncalls) {
 uint64_t ozaki2_launch_count(void) { return g_launches.load(); }
 
 oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
-                              const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                              const double* B, int64_t ldb, double* C, int64_t ldc, int s, oz2_mode mode,
                               void* stream, int32_t* alpha, int32_t* beta, int8_t* Ares,
                               int8_t* Bres, int32_t* P, uint8_t* R, uint64_t* X) {
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
@@ -849,7 +849,7 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r, const double* A, 
 }
 
 oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
-                               const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                               const double* B, int64_t ldb, double* C, int64_t ldc, int s, oz2_mode mode,
                                void* stream, float* stage_ms) {
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
   if (e != OZ2_OK) return e;
@@ -870,7 +870,7 @@ oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r, const double* A,
 }
 
 oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda,
-                             const double* B, int64_t ldb, double* C, int64_t ldc, int s, int mode,
+                             const double* B, int64_t ldb, double* C, int64_t ldc, int s, oz2_mode mode,
                              void* stream) {
   oz2_status e = check_args(p, q, r, A, lda, B, ldb, C, ldc, s, mode);
   if (e != OZ2_OK) return e;

@@ -95,7 +95,7 @@ oz2_status ozaki2_dgemm(int64_t p, int64_t q, int64_t r,
                         const double* A, int64_t lda,
                         const double* B, int64_t ldb,
                         double* C, int64_t ldc,
-                        int s, int mode, void* stream);
+                        int s, oz2_mode mode, void* stream);
 
 /*
  * The same pipeline, run by the same kernels, with each stage's output
@@ -117,7 +117,7 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r,
                               const double* A, int64_t lda,
                               const double* B, int64_t ldb,
                               double* C, int64_t ldc,
-                              int s, int mode, void* stream,
+                              int s, oz2_mode mode, void* stream,
                               int32_t* alpha, int32_t* beta,
                               int8_t* Ares, int8_t* Bres,
                               int32_t* P, uint8_t* R, uint64_t* X);
@@ -138,7 +138,7 @@ oz2_status ozaki2_dgemm_stages(int64_t p, int64_t q, int64_t r,
                                const double* A, int64_t lda,
                                const double* B, int64_t ldb,
                                double* C, int64_t ldc,
-                               int s, int mode, void* stream, float* stage_ms);
+                               int s, oz2_mode mode, void* stream, float* stage_ms);
 
 /*
  * Host-memory variant: A, B and C are HOST pointers (pinned memory gives the
@@ -153,7 +153,7 @@ oz2_status ozaki2_dgemm_host(int64_t p, int64_t q, int64_t r,
                              const double* A, int64_t lda,
                              const double* B, int64_t ldb,
                              double* C, int64_t ldc,
-                             int s, int mode, void* stream);
+                             int s, oz2_mode mode, void* stream);
 
 /*
  * Stage profiling.  After ozaki2_profile_begin(max_calls), each of the next

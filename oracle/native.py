@@ -60,6 +60,10 @@ def _load():
     lib.oz2o_products.restype = i32
     lib.oz2o_crt.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, i64]
     lib.oz2o_crt.restype = i32
+    lib.oz2o_exponents.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, i32, i32, vp, vp]
+    lib.oz2o_exponents.restype = i32
+    lib.oz2o_entries.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, vp, vp, i64, vp, vp, i32, vp, vp, vp]
+    lib.oz2o_entries.restype = i32
     lib.oz2o_exact_entries.argtypes = [i64, i64, i64, vp, i64, vp, i64, i64, vp, vp, i32, vp, vp, vp, vp, i32]
     lib.oz2o_exact_entries.restype = i32
     _lib = lib
@@ -169,6 +173,45 @@ def dgemm_all_in_c(A, B, s: int, mode: str, nthreads: int | None = None) -> dict
     return o
 
 
+def exponents(A, B, s: int, mode: str, nthreads: int | None = None):
+    """(alpha, beta): the row and column exponents of the native oracle."""
+    A = _colmajor(A)
+    B = _colmajor(B)
+    p, q = A.shape
+    r = B.shape[1]
+    alpha = np.empty(p, dtype=np.int32)
+    beta = np.empty(r, dtype=np.int32)
+    rc = _load().oz2o_exponents(p, q, r, A.ctypes.data, p, B.ctypes.data, q, int(s), {"fast": 0, "accu": 1}[mode],
+                                nthreads or threads(), alpha.ctypes.data, beta.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"native oracle refused the problem (code {rc})")
+    return alpha, beta
+
+
+def entries(A, B, s: int, alpha, beta, ii, jj, nthreads: int | None = None) -> dict:
+    """The pipeline at sampled outputs (ii[k], jj[k]) only, given the exponents.
+
+    Returns R [n, s] uint8, X [n, 3] uint64 (192-bit two's complement) and C [n]."""
+    A = _colmajor(A)
+    B = _colmajor(B)
+    p, q = A.shape
+    r = B.shape[1]
+    alpha = np.ascontiguousarray(alpha, dtype=np.int32)
+    beta = np.ascontiguousarray(beta, dtype=np.int32)
+    ii = np.ascontiguousarray(ii, dtype=np.int64)
+    jj = np.ascontiguousarray(jj, dtype=np.int64)
+    n = ii.shape[0]
+    R = np.empty((n, s), dtype=np.uint8)
+    X = np.empty((n, 3), dtype=np.uint64)
+    C = np.empty(n, dtype=np.float64)
+    rc = _load().oz2o_entries(p, q, r, A.ctypes.data, p, B.ctypes.data, q, int(s), alpha.ctypes.data,
+                              beta.ctypes.data, n, ii.ctypes.data, jj.ctypes.data, nthreads or threads(),
+                              R.ctypes.data, X.ctypes.data, C.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"native oracle refused the entries (code {rc})")
+    return {"R": R, "X": X, "C": C}
+
+
 def exact_entries(A, B, ii, jj, Chats=(), nthreads: int | None = None):
     """Exact dot products at the sampled outputs (ii[k], jj[k]), each rounded once.
 
@@ -203,20 +246,17 @@ def _norm2(x):
     return m * float(np.sqrt(np.sum((x / m) ** 2)))
 
 
-def accuracy(A, B, Cs: dict, ii=None, jj=None) -> dict:
-    """Errors of each product in Cs (name -> full (p, r) array) against the exact AB.
+def accuracy_at(A, B, ii, jj, values: dict) -> dict:
+    """Errors against the exact AB at the entries (ii[k], jj[k]).
 
-    normwise      = ||C_hat - AB||_F / ||AB||_F,
-    componentwise = max_ij |C_hat - AB|_ij / (|A||B|)_ij   (entries with (|A||B|)_ij > 0),
-    over every entry, or over the sampled entries (ii, jj) when given."""
-    p, r = np.shape(A)[0], np.shape(B)[1]
-    if ii is None:
-        jj_g, ii_g = np.meshgrid(np.arange(r), np.arange(p))
-        ii, jj = ii_g.ravel(), jj_g.ravel()
-    names = list(Cs)
-    vals = [np.asarray(Cs[k])[ii, jj] for k in names]
-    exact, absprod, errs = exact_entries(A, B, ii, jj, vals)
-    out = {"entries": int(len(ii))}
+    values: name -> the product's values at those entries.  For each name:
+    normwise      = ||C_hat - AB|| / ||AB||   (2-norms over the entries),
+    componentwise = max |C_hat - AB|_ij / (|A||B|)_ij over entries with (|A||B|)_ij > 0
+                    (inf if C_hat is nonzero where |A||B| is zero),
+    max_abs_err   = max |C_hat - AB|_ij."""
+    names = list(values)
+    exact, absprod, errs = exact_entries(A, B, ii, jj, [values[k] for k in names])
+    out = {"entries": int(len(exact))}
     den = _norm2(exact)
     pos = absprod > 0
     for k, e in zip(names, errs):
@@ -226,3 +266,11 @@ def accuracy(A, B, Cs: dict, ii=None, jj=None) -> dict:
         out[k] = {"normwise": _norm2(e) / den if den > 0 else _norm2(e),
                   "componentwise": comp, "max_abs_err": float(np.max(np.abs(e))) if e.size else 0.0}
     return out
+
+
+def accuracy(A, B, Cs: dict) -> dict:
+    """accuracy_at over every entry of the full (p, r) products in Cs."""
+    p, r = np.shape(A)[0], np.shape(B)[1]
+    jj_g, ii_g = np.meshgrid(np.arange(r), np.arange(p))
+    ii, jj = ii_g.ravel(), jj_g.ravel()
+    return accuracy_at(A, B, ii, jj, {k: np.asarray(v)[ii, jj] for k, v in Cs.items()})

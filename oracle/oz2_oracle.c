@@ -41,12 +41,16 @@
  *
  * Entry points (plain C; pointers are host memory; matrices column-major):
  *   int oz2o_moduli(int s, int32_t* out);
+ *   int oz2o_exponents(p, q, r, A, lda, B, ldb, s, mode, nthreads,
+ *                      alpha, beta);                        O2
  *   int oz2o_residues(p, q, r, A, lda, B, ldb, s, mode, nthreads,
  *                     alpha, beta, Ares, Bres);             O2-O4
  *   int oz2o_products(p, q, r, s, nthreads, Ares, Bres, R);   O5-O6
  *   int oz2o_crt(p, r, s, nthreads, R, alpha, beta, X, C, ldc); O7-O8
  *   int oz2o_dgemm(p, q, r, A, lda, B, ldb, s, mode, nthreads,
  *                  alpha, beta, Ares, Bres, R, X, C, ldc);    all of them
+ *   int oz2o_entries(p, q, r, A, lda, B, ldb, s, alpha, beta, n, ii, jj,
+ *                    nthreads, R, X, C);            O3-O8 at sampled entries
  *   int oz2o_exact_entries(p, q, r, A, lda, B, ldb, n, ii, jj, nc, Chat,
  *                          exact, absprod, err, nthreads);
  * They return 0, or a negative code for bad arguments (-1), a bound the
@@ -683,41 +687,50 @@ int oz2o_moduli(int s, int32_t* out) {
   return s;
 }
 
-/* O2-O4: exponents and residue planes (all four outputs required) */
-int oz2o_residues(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda, const double* B, int64_t ldb,
-                  int s, int mode, int nthreads, int32_t* alpha, int32_t* beta, int8_t* Ares, int8_t* Bres) {
-  if (p <= 0 || q <= 0 || r <= 0 || lda < p || ldb < q || !A || !B) return -1;
-  if (!alpha || !beta || !Ares || !Bres) return -1;
+/* O2: the exponents alpha [p], beta [r] */
+int oz2o_exponents(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda, const double* B, int64_t ldb,
+                   int s, int mode, int nthreads, int32_t* alpha, int32_t* beta) {
+  if (p <= 0 || q <= 0 || r <= 0 || lda < p || ldb < q || !A || !B || !alpha || !beta) return -1;
   if (mode != 0 && mode != 1) return -1;
   if (mode == 0 && q >= (1 << 24)) return -2;                        /* the exact statistic: q 2^40 < 2^64 */
   if (mode == 1 && (int64_t)q * 127 * 127 >= (1ll << 31)) return -2; /* Wbar in INT32 */
   consts c;
   if (make_consts(s, &c) != 0) return -1;
   expctx ex = {p, q, r, lda, ldb, A, B, &c, alpha, beta, NULL, NULL, NULL, NULL, NULL};
-  int rc = 0;
   if (mode == 0) {
     run_tasks(fast_task, &ex, p + r, nthreads);
-  } else {
-    ex.u = (int32_t*)malloc(sizeof(int32_t) * p);
-    ex.v = (int32_t*)malloc(sizeof(int32_t) * r);
-    ex.Abar = (uint8_t*)malloc((size_t)p * q);
-    ex.Bbar = (uint8_t*)malloc((size_t)r * q);
-    ex.W = (int32_t*)malloc(sizeof(int32_t) * p * r);
-    if (ex.u && ex.v && ex.Abar && ex.Bbar && ex.W) {
-      run_tasks(bound_quant_task, &ex, p + r, nthreads);
-      bmmctx bm = {p, q, r, ex.Abar, ex.Bbar, ex.W};
-      run_tasks(bmm_task, &bm, ((p + BI - 1) / BI) * ((r + BJ - 1) / BJ), nthreads);
-      run_tasks(accu_exp_task, &ex, p + r, nthreads);
-    } else {
-      rc = -3;
-    }
-    free(ex.u);
-    free(ex.v);
-    free(ex.Abar);
-    free(ex.Bbar);
-    free(ex.W);
-    if (rc) return rc;
+    return 0;
   }
+  int rc = 0;
+  ex.u = (int32_t*)malloc(sizeof(int32_t) * p);
+  ex.v = (int32_t*)malloc(sizeof(int32_t) * r);
+  ex.Abar = (uint8_t*)malloc((size_t)p * q);
+  ex.Bbar = (uint8_t*)malloc((size_t)r * q);
+  ex.W = (int32_t*)malloc(sizeof(int32_t) * p * r);
+  if (ex.u && ex.v && ex.Abar && ex.Bbar && ex.W) {
+    run_tasks(bound_quant_task, &ex, p + r, nthreads);
+    bmmctx bm = {p, q, r, ex.Abar, ex.Bbar, ex.W};
+    run_tasks(bmm_task, &bm, ((p + BI - 1) / BI) * ((r + BJ - 1) / BJ), nthreads);
+    run_tasks(accu_exp_task, &ex, p + r, nthreads);
+  } else {
+    rc = -3;
+  }
+  free(ex.u);
+  free(ex.v);
+  free(ex.Abar);
+  free(ex.Bbar);
+  free(ex.W);
+  return rc;
+}
+
+/* O2-O4: exponents and residue planes (all four outputs required) */
+int oz2o_residues(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda, const double* B, int64_t ldb,
+                  int s, int mode, int nthreads, int32_t* alpha, int32_t* beta, int8_t* Ares, int8_t* Bres) {
+  if (!Ares || !Bres) return -1;
+  int rc = oz2o_exponents(p, q, r, A, lda, B, ldb, s, mode, nthreads, alpha, beta);
+  if (rc != 0) return rc;
+  consts c;
+  make_consts(s, &c);
   resctx rs = {p, q, r, lda, ldb, A, B, &c, alpha, beta, Ares, Bres};
   run_tasks(res_task, &rs, p + r, nthreads);
   return 0;
@@ -776,6 +789,66 @@ int oz2o_dgemm(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda, co
   if (!Bres_out) free(Bres);
   if (!R_out) free(R);
   return rc;
+}
+
+/* O3-O8 at sampled outputs (ii[k], jj[k]) only, given the exponents: the
+ * residues of row i of A and column j of B are formed on the fly, then
+ * P_t = sum_l rho(a'_il) rho(b'_lj), R_t, X and C as above.  Outputs:
+ * R [n][s] (may be NULL), X [n][3], C [n]. */
+typedef struct {
+  int64_t q, lda, ldb;
+  const double* A;
+  const double* B;
+  const consts* c;
+  const int32_t* alpha;
+  const int32_t* beta;
+  const int64_t* ii;
+  const int64_t* jj;
+  uint8_t* R;
+  uint64_t* X;
+  double* C;
+} entctx;
+
+static void entry_task(void* ctx, int64_t k) {
+  entctx* x = (entctx*)ctx;
+  const consts* c = x->c;
+  int64_t i = x->ii[k], j = x->jj[k];
+  int64_t P[SMAX] = {0};
+  for (int64_t l = 0; l < x->q; ++l) {
+    int na, nb, Ea, Eb;
+    uint64_t ma, mb;
+    decompose(x->A[l * x->lda + i], &na, &ma, &Ea);
+    decompose(x->B[j * x->ldb + l], &nb, &mb, &Eb);
+    for (int t = 0; t < c->s; ++t) {
+      uint32_t m = (uint32_t)c->m[t];
+      int64_t ra = (int64_t)trunc_mod(ma, Ea + x->alpha[i], m);
+      int64_t rb = (int64_t)trunc_mod(mb, Eb + x->beta[j], m);
+      P[t] += (int64_t)centered(na ? -ra : ra, (int)m) * centered(nb ? -rb : rb, (int)m);
+    }
+  }
+  uint8_t Rk[SMAX];
+  for (int t = 0; t < c->s; ++t) {
+    int64_t v = P[t] % c->m[t];
+    Rk[t] = (uint8_t)(v < 0 ? v + c->m[t] : v);
+    if (x->R) x->R[k * c->s + t] = Rk[t];
+  }
+  /* the CRT of one entry: the same steps as crt_task on a one-entry R */
+  crtctx one = {1, 1, 1, c, Rk, x->alpha + i, x->beta + j, x->X + k * 3, x->C + k};
+  crt_task(&one, 0);
+}
+
+int oz2o_entries(int64_t p, int64_t q, int64_t r, const double* A, int64_t lda, const double* B, int64_t ldb,
+                 int s, const int32_t* alpha, const int32_t* beta, int64_t n, const int64_t* ii,
+                 const int64_t* jj, int nthreads, uint8_t* R, uint64_t* X, double* C) {
+  if (p <= 0 || q <= 0 || r <= 0 || lda < p || ldb < q || !A || !B || !alpha || !beta) return -1;
+  if (n < 0 || (n > 0 && (!ii || !jj || !X || !C))) return -1;
+  for (int64_t k = 0; k < n; ++k)
+    if (ii[k] < 0 || ii[k] >= p || jj[k] < 0 || jj[k] >= r) return -1;
+  consts c;
+  if (make_consts(s, &c) != 0) return -1;
+  entctx e = {q, lda, ldb, A, B, &c, alpha, beta, ii, jj, R, X, C};
+  run_tasks(entry_task, &e, n, nthreads);
+  return 0;
 }
 
 /* ------------------------------------------------------------------ exact dot products */

@@ -34,8 +34,15 @@ def test_moduli_match_oracle(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
-        assert lib.ozaki2_status_string(code)
+    # every code of oz2_status (include/ozaki2.h) has its own text, and the binding names it
+    texts = [lib.ozaki2_status_string(code) for code in range(8)]
+    assert all(texts) and len(set(texts)) == 8
+    assert lib.ozaki2_status_string(8) == b"unknown status"
+    assert sorted(oz2.STATUS) == list(range(8))
+    import re
+    header = open(oz2.library_path().replace("emulated_fp64_gemm_gb300/libozaki2.so", "include/ozaki2.h")).read()
+    enum = dict((int(v), k) for k, v in re.findall(r"\b(OZ2_(?:OK|ERR_\w+))\s*=\s*(\d+)", header))
+    assert enum == oz2.STATUS
 
 
 def _call(lib, p=4, q=4, r=4, A=1, lda=4, B=1, ldb=4, C=1, ldc=4, s=8, mode=0):

@@ -84,3 +84,44 @@ def test_max_over_two_gloo_ranks():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 15.0), (1, 15.0)]
+
+
+def test_stage_work_counts_what_each_stage_runs():
+    w = bench.WORKLOADS["n8192_s14_fast"]
+    n2 = 8192 * 8192
+    work = bench.stage_work(w)
+    # q = 8192: A's statistics read A once; B's one-read kernel makes B's planes in this stage
+    assert work["scale"] == ("hbm", float(8 * n2 + (8 + 2 * 14) * n2))
+    assert work["residues"] == ("hbm", float((8 + 2 * 14) * n2))
+    assert work["crt"] == ("hbm", float((14 + 8) * n2))
+    assert work["gemm_mod"] == ("tensor", 2.0 * 14 * n2 * 8192)
+    assert work["bound_gemm"][1] == 0.0
+    small = bench.dataclasses.replace(w, p=1024, q=1024, r=1024)  # both one-read kernels
+    ws = bench.stage_work(small)
+    assert ws["residues"][1] == 0.0 and ws["scale"][1] == float((8 + 28) * 2 * 1024 * 1024)
+    acc = bench.WORKLOADS["n4096_s14_accu"]
+    wa = bench.stage_work(acc)
+    assert wa["scale"][1] == float(10 * 2 * 4096 * 4096) and wa["bound_gemm"][1] == 2.0 * 4096**3
+
+
+def test_stage_roofline_flags_rates_above_the_peak():
+    w = bench.WORKLOADS["n8192_s14_fast"]
+    work = bench.stage_work(w)
+    ms_ok = {"scale": work["scale"][1] / 5e9 * 1e3 / 1e3, "residues": 0.2, "gemm_mod": 9.0, "crt": 0.5}
+    out = bench.stage_roofline(w, ms_ok, 6792.1, 1898.6)
+    assert set(out) == {"scale", "residues", "gemm_mod", "crt"}
+    assert abs(out["scale"]["GBps"] - 5000.0) < 1e-6 and not out["scale"]["suspect"]
+    assert abs(out["crt"]["frac"] - (22 * 8192**2 / 0.5e-3 / 1e9) / 6792.1) < 1e-12
+    fast = bench.stage_roofline(w, {"crt": 0.05}, 6792.1, 1898.6)
+    assert fast["crt"]["suspect"]  # 29 TB/s: the timing cannot cover the work
+
+
+def test_s_and_mode_overrides_rename_the_workload():
+    args = bench.parse_args(["--workload", "n8192_s14_fast", "--s", "18", "--mode", "accu"])
+    w = bench.resolve_workload(args)
+    assert (w.name, w.s, w.mode, w.p) == ("n8192_s18_accu", 18, "accu", 8192)
+    line = bench.result_line(value=1.0, n_gpus=1, steps=1, warmup=3, ms_per_step=1.0, workload=w, extra={})
+    assert line["config"]["workload"] == "n8192_s18_accu" and "s=18 accu" in line["metric"]
+    assert line["vs_baseline"] is None
+    same = bench.resolve_workload(bench.parse_args([]))
+    assert same is bench.WORKLOADS["n8192_s14_fast"]

@@ -158,7 +158,7 @@ def test_accuracy_report_on_exact_and_perturbed_products():
     assert rep["bad"]["componentwise"] == pytest.approx(1.0 / absAB[3, 4], rel=1e-15)
     assert rep["bad"]["normwise"] == pytest.approx(1.0 / np.linalg.norm(C), rel=1e-12)
     # sampled entries
-    rep2 = native.accuracy(A, B, {"bad": bad}, ii=np.array([3, 0]), jj=np.array([4, 0]))
+    rep2 = native.accuracy_at(A, B, np.array([3, 0]), np.array([4, 0]), {"bad": bad[[3, 0], [4, 0]]})
     assert rep2["entries"] == 2 and rep2["bad"]["max_abs_err"] == 1.0
 
 
@@ -183,3 +183,22 @@ def test_product_paths_and_entry_points_agree(mode):
     for k in native.OUTPUTS:
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
         np.testing.assert_array_equal(a[k], c[k], err_msg=k)
+
+
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+def test_sampled_entries_and_exponents_match_the_full_path(mode):
+    A, B = make_matrices(70, 300, 50, 2.0, 71)
+    A[5, :] *= 1e-310
+    A[6, 3] = 1e300
+    B[:, 7] = 0.0
+    full = native.dgemm(A, B, 18, mode)
+    al, be = native.exponents(A, B, 18, mode)
+    np.testing.assert_array_equal(al, full["alpha"])
+    np.testing.assert_array_equal(be, full["beta"])
+    rng = np.random.default_rng(1)
+    ii = np.concatenate([rng.integers(0, 70, 200), [0, 69, 5, 6]])
+    jj = np.concatenate([rng.integers(0, 50, 200), [49, 0, 7, 7]])
+    e = native.entries(A, B, 18, al, be, ii, jj)
+    np.testing.assert_array_equal(e["R"], full["R"][:, jj, ii].T)
+    np.testing.assert_array_equal(e["X"], full["X"][jj, ii])
+    np.testing.assert_array_equal(e["C"], full["C"][ii, jj])

@@ -74,3 +74,51 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     rc = lib.ozaki2_fast_exponents_noalloc(MAX_VECTORS, 1, 1, dA.data_ptr(), MAX_VECTORS,
                                            dA.data_ptr(), 1, 14, out.data_ptr(), out.data_ptr(), st)
     assert rc == OZ2_ERR_SCRATCH_TOO_SMALL
+
+
+def test_noalloc_call_leaves_free_device_memory_unchanged(lib):
+    """After a first call (which looks up the scratch array and loads the
+    kernels), a further call must not change the device's free memory: it
+    allocates nothing, neither through the CUDA runtime nor through torch."""
+    A, B = make_matrices(640, 512, 384, 1.0, 13)
+    dA, dB = _dev(A), _dev(B)
+    alpha = torch.empty(640, dtype=torch.int32, device="cuda")
+    beta = torch.empty(384, dtype=torch.int32, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        rc = lib.ozaki2_fast_exponents_noalloc(640, 512, 384, dA.data_ptr(), dA.stride(1), dB.data_ptr(),
+                                               dB.stride(1), 14, alpha.data_ptr(), beta.data_ptr(), st)
+        assert rc == 0
+        torch.cuda.synchronize()
+
+    call()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    for _ in range(3):
+        call()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_reserved() == reserved0
+
+
+def test_noalloc_at_its_scratch_limit(lib):
+    """p + r equal to the limit is accepted and gives the pipeline's exponents."""
+    import emulated_fp64_gemm_gb300 as oz2
+
+    r = 8
+    p = MAX_VECTORS - r
+    rng = np.random.default_rng(14)
+    A = (rng.random((p, 3)) - 0.5) * np.exp(rng.standard_normal((p, 3)))
+    B = (rng.random((3, r)) - 0.5) * np.exp(rng.standard_normal((3, r)))
+    dA, dB = _dev(A), _dev(B)
+    got_a, got_b = _noalloc(lib, dA, dB, 14)
+    ref = oz2.dgemm_debug(dA, dB, 14, "fast", want_p=False)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got_a, ref["alpha"].cpu().numpy())
+    np.testing.assert_array_equal(got_b, ref["beta"].cpu().numpy())
+    # one more vector is refused before anything is enqueued
+    out = torch.zeros(8, dtype=torch.int32, device="cuda")
+    rc = lib.ozaki2_fast_exponents_noalloc(p + 1, 3, r, dA.data_ptr(), p + 1, dB.data_ptr(), 3, 14,
+                                           out.data_ptr(), out.data_ptr(), ctypes.c_void_p(0))
+    assert rc == OZ2_ERR_SCRATCH_TOO_SMALL
