@@ -81,6 +81,8 @@ def parse_args(argv=None):
     ap.add_argument("--mode", choices=["fast", "accu"], default=None, help="bound mode (overrides the workload's)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every s in %s at n in %s, fast and accu (one JSON line each)" % (SWEEP_S, SWEEP_N))
+    ap.add_argument("--stages-once", action="store_true",
+                    help="one call of the stage-timed entry point (each stage alone), e.g. under a profiler")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true",
@@ -650,10 +652,32 @@ def run_sweep(args):
     return 0
 
 
+def run_stages_once(args):
+    """One ozaki2_dgemm_stages call on the workload (stages one after another)."""
+    import torch
+
+    import __graft_entry__ as entry
+
+    entry.build()
+    import emulated_fp64_gemm_gb300 as oz2
+
+    w = resolve_workload(args)
+    A, B = make_workload(w)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    _, ms = oz2.dgemm_stages(dA, dB, w.s, w.mode)
+    torch.cuda.synchronize()
+    status = oz2.last_error()
+    print(json.dumps({"workload": w.name, "stages_ms": ms, "last_error": status}), flush=True)
+    return 0 if status == 0 else 1
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_setup()
-    if args.sweep:
+    if args.stages_once:
+        rc = run_stages_once(args) if rank == 0 else 0
+    elif args.sweep:
         rc = run_sweep(args) if rank == 0 else 0
     elif args.impl == "reference":
         rc = run_reference(args, rank)

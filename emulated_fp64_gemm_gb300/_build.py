@@ -15,7 +15,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 LIB_PATH = os.path.join(PKG_DIR, "libozaki2.so")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
-SOURCES = ["oz2_api.cu", "oz2_prep.cu", "oz2_gemm.cu", "oz2_crt.cu", "oz2_noalloc.cu"]
+SOURCES = ["oz2_api.cu", "oz2_prep.cu", "oz2_residue.cu", "oz2_gemm.cu", "oz2_crt.cu", "oz2_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -563,7 +563,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
       if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[0], 0));  // one part: all of B
       OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,
                                         wsp->aux));
-      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, r, hc->mod, beta, ds->pow2mod, max_bits, planesB, wsp->aux));
     }
     OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
     b_side_done = true;
@@ -647,7 +647,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     if (!a_planes_done)
       OZ2_CU(launch_residues_rows(A, p, q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits, planesA, st));
     if (!b_planes_done)
-      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, r, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[3], st));
     g.p = p;
     g.row0 = 0;
@@ -660,7 +660,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
   } else {
     cudaStream_t aux = wsp->aux;
     if (!b_side_done)
-      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
+      OZ2_CU(launch_residues_cols(B, q, r, ldb, qp, r, hc->mod, beta, ds->pow2mod, max_bits, planesB, st));
     if (!fused_a)  // (with fused_a block 0's planes came with its statistics)
       OZ2_CU(launch_residues_rows(A, rows_of(0), q, lda, qp, p, hc->mod, alpha, ds->pow2mod, max_bits,
                                   planesA, st));

@@ -112,16 +112,19 @@ cudaError_t launch_residues_rows(const double* A, int64_t rows, int64_t q, int64
                                  int64_t plane_rows, const ModConsts& mc, const int32_t* alpha,
                                  const uint8_t* pow2mod, int max_bits, uint16_t* planes,
                                  cudaStream_t st);
-// residue planes of B (column-major q x r) into fp16 planes [s][r][qp].
-cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t r, int64_t ldb, int64_t qp,
-                                 const ModConsts& mc, const int32_t* beta, const uint8_t* pow2mod,
-                                 int max_bits, uint16_t* planes, cudaStream_t st);
+// residue planes of `ncols` columns of B (column-major, leading dimension ldb)
+// into fp16 planes [s][plane_cols][qp]; B, beta and planes point at the first
+// column.
+cudaError_t launch_residues_cols(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
+                                 int64_t plane_cols, const ModConsts& mc, const int32_t* beta,
+                                 const uint8_t* pow2mod, int max_bits, uint16_t* planes, cudaStream_t st);
 
-// fast mode, B side in one read of B: beta and the residue planes of `ncols`
-// columns (identical to launch_fast_exponents_cols followed by
-// launch_residues_cols); B, beta and planes point at the first column, plane
-// rows are plane_cols apart ([s][plane_cols][qp]).  For q <= 8192 only
-// (cols_fused_fast_supported).
+// fast mode, B side: beta and the residue planes of `ncols` columns
+// (identical to launch_fast_exponents_cols followed by launch_residues_cols);
+// B, beta and planes point at the first column, plane rows are plane_cols
+// apart ([s][plane_cols][qp]).  For q <= 8192 only (cols_fused_fast_supported):
+// up to q = 2048 one kernel reads B once for both, above that the statistics
+// take one read of B and the residues a second.
 bool cols_fused_fast_supported(int64_t q);
 cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
                                    int64_t plane_cols, const BoundConsts& bc, const ModConsts& mc,
