@@ -126,8 +126,9 @@ oz2_status ozaki2_dgemm_debug(int64_t p, int64_t q, int64_t r,
  * ozaki2_dgemm with CUDA events recorded between its stages; synchronises
  * `stream` and writes the milliseconds of each stage to stage_ms[0..5]:
  *   0 scale statistics and exponents (fast) or bound quantisation (accu);
- *     in fast mode with q <= 8192 also B's residue planes, which one kernel
- *     produces together with B's statistics in a single read of B
+ *     in fast mode with q <= 8192 also B's residue planes, made together
+ *     with B's statistics (one kernel reading B once up to q = 2048; above
+ *     that a statistics kernel, then the residue kernel)
  *   1 bound GEMM and exponents (accu; 0 in fast mode)
  *   2 residue planes of A and (unless made in stage 0) of B
  *   3 the s modular GEMMs with the fused mod-m_t epilogue
