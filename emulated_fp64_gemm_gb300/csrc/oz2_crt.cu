@@ -167,8 +167,13 @@ __device__ __forceinline__ double crt_round_x(uint32_t (&X)[NL], const CrtConsts
 // p_total rows per column.  Thread = (row i, group of 4 columns); x walks the
 // rows, y a strided set of column groups.  NBC: the byte limbs of the largest
 // M/m_t for s <= MAXS (s - 1 for s >= 5); the dp4a loop stops there.
-template <int MAXS, int NL16, int NBC>
-__global__ void __launch_bounds__(256) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
+// MINB: resident blocks per SM the register allocation must allow.  The
+// kernel is latency-bound (long dependent chains per output), so occupancy
+// pays even with a few spilled registers: at 8192^2, s = 14 three blocks per
+// SM took 707 -> 612 us, and at s = 18 four blocks 919 -> 880 us; at s = 8 the
+// unconstrained allocation already fits four.
+template <int MAXS, int NL16, int NBC, int MINB>
+__global__ void __launch_bounds__(256, MINB) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
                                                   int64_t jg0, int64_t jg1, int64_t r,
                                                   const __grid_constant__ CrtConsts cc,
                                                   const uint8_t* __restrict__ Wb,
@@ -292,12 +297,12 @@ cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t col0
   const int nl = crt_limbs(s);
   // exact instances for the common channel counts (fewer groups and byte
   // limbs), else the limb-count buckets with MAXS - 1 coefficient bytes
-  if (s == 8) crt_kernel<8, 6, 7><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (s == 14) crt_kernel<14, 8, 13><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (s == 18) crt_kernel<18, 10, 17><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 3) crt_kernel<11, 6, 10><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 4) crt_kernel<15, 8, 14><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else crt_kernel<20, 10, 19><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  if (s == 8) crt_kernel<8, 6, 7, 1><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (s == 14) crt_kernel<14, 8, 13, 3><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (s == 18) crt_kernel<18, 10, 17, 4><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 3) crt_kernel<11, 6, 10, 1><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else if (nl == 4) crt_kernel<15, 8, 14, 3><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+  else crt_kernel<20, 10, 19, 4><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
   count_launches(1);
   return cudaGetLastError();
 }

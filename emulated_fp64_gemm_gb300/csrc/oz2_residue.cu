@@ -13,8 +13,8 @@
 // (8, 14 or 20 channels, every s rounded up to the next bucket): the loop
 // unrolls, each modulus' constants are immediate kernel-parameter operands,
 // and channels past s are skipped by a uniform branch.  At the headline
-// shape (8192 x 8192, s = 14) this took A's residue kernel from 0.68 to 0.81
-// of the measured HBM copy peak, and B's from 0.81 to 0.93.
+// shape (8192 x 8192, s = 14, each kernel alone) this took A's residue kernel
+// from 0.68 to 0.77 of the measured HBM copy peak, and B's from 0.81 to 0.89.
 #include <algorithm>
 
 #include "oz2_bits.cuh"
@@ -384,13 +384,18 @@ __global__ void __launch_bounds__(256, 3) fused_cols_fast_kernel(const double* _
 
 // Fast mode, A side for short rows in one read of A: statistics, exponent
 // alpha_i and residue planes of R rows per block.  Thread t holds row t % R's
-// columns [8 s + 8 S c, +8) for c < 4 (s = t / R, S = 256 / R column slots), so
-// q <= 8192 / R; the per-row max and sum of squares reduce over the lanes that
-// share a row and then over the warps, with no atomics and nothing to clear.
-// Results are identical to the per-row-block path (amax_rows, sumsq_rows +
-// fast_exp, residue_rows).
-template <int R, int SB, int NW>
-__global__ void __launch_bounds__(256, 1) fused_rows_fast_kernel(const double* __restrict__ A, int64_t rows,
+// columns [8 s + 8 S c, +8) for c < NCH (s = t / R, S = 256 / R column slots),
+// so q <= 8 S NCH; the per-row max and sum of squares reduce over the lanes
+// that share a row and then over the warps, with no atomics and nothing to
+// clear.  Results are identical to the per-row-block path (amax_rows,
+// sumsq_rows + fast_exp, residue_rows).  R = 4 rows per block: every load
+// instruction of a warp reads 32 bytes (one sector) from each of 8 columns.
+template <int NCH>
+struct FusedRowsOcc {
+  static constexpr int kMinBlocks = NCH <= 2 ? 2 : 1;
+};
+template <int R, int NCH, int SB, int NW>
+__global__ void __launch_bounds__(256, FusedRowsOcc<NCH>::kMinBlocks) fused_rows_fast_kernel(const double* __restrict__ A, int64_t rows,
                                                               int64_t q, int64_t lda, int64_t qp,
                                                               int64_t plane_rows, BoundConsts bc,
                                                               const __grid_constant__ ModConsts mc,
@@ -398,7 +403,6 @@ __global__ void __launch_bounds__(256, 1) fused_rows_fast_kernel(const double* _
                                                               int32_t* __restrict__ alpha,
                                                               uint16_t* __restrict__ planes) {
   constexpr int S = 256 / R;  // column slots per row
-  constexpr int NCH = 4;      // 8-column chunks per thread
   __shared__ uint64_t red[8][R];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = tid % R, cs = tid / R;
@@ -513,16 +517,20 @@ cudaError_t launch_rows_fused_fast(const double* A, int64_t rows, int64_t q, int
                                    const uint8_t* pow2mod, int max_bits, int32_t* alpha, uint16_t* planes,
                                    cudaStream_t st) {
   if (!rows_fused_fast_supported(q) || rows < 1) return cudaErrorInvalidValue;
-  const int R = (qp <= 1024) ? 8 : 4;
-  const dim3 g(static_cast<unsigned>((rows + R - 1) / R));
+  // four rows per block, 64 column slots of 8: 1, 2 or 4 register chunks per thread
+  const int nch = qp <= 512 ? 1 : (qp <= 1024 ? 2 : 4);
+  const dim3 g(static_cast<unsigned>((rows + 3) / 4));
 #define OZ2_L(SB, NW)                                                                                          \
   do {                                                                                                         \
-    if (R == 8)                                                                                                \
-      fused_rows_fast_kernel<8, SB, NW><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, \
-                                                           planes);                                           \
+    if (nch == 1)                                                                                              \
+      fused_rows_fast_kernel<4, 1, SB, NW><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, \
+                                                              alpha, planes);                                 \
+    else if (nch == 2)                                                                                         \
+      fused_rows_fast_kernel<4, 2, SB, NW><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, \
+                                                              alpha, planes);                                 \
     else                                                                                                       \
-      fused_rows_fast_kernel<4, SB, NW><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, alpha, \
-                                                           planes);                                           \
+      fused_rows_fast_kernel<4, 4, SB, NW><<<g, 256, 0, st>>>(A, rows, q, lda, qp, plane_rows, bc, mc, pow2mod, \
+                                                              alpha, planes);                                 \
   } while (0)
   OZ2_RES_DISPATCH(max_bits, mc.s, OZ2_L);
 #undef OZ2_L
