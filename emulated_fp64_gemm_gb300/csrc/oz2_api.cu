@@ -140,7 +140,6 @@ const Tables& tables() {
         Big Mt = M;
         const uint32_t rem = big_divmod_small(Mt, m);
         (void)rem;  // M is a multiple of m
-        for (int k = 0; k < kLimbs16; ++k) cc.Mt16[t][k] = (Mt.l[k / 2] >> (16 * (k % 2))) & 0xFFFFu;
         Big tmp = Mt;
         const uint32_t mt_mod = big_divmod_small(tmp, m);
         uint32_t inv = 0;
@@ -156,12 +155,14 @@ const Tables& tables() {
       Big Mh = M;
       big_divmod_small(Mh, 2);
       for (int k = 0; k < kLimbs; ++k) cc.Mhalf[k] = Mh.l[k];
-      for (int k = 0; k < kLimbs16; ++k) cc.M16[k] = (M.l[k / 2] >> (16 * (k % 2))) & 0xFFFFu;
-      const int nl16 = 2 * crt_limbs(s);
-      double mest = 0.0;
-      for (int k = (nl16 > 6 ? nl16 - 6 : 0); k < nl16; ++k)  // the limbs the kernel's estimate uses
-        mest += static_cast<double>(cc.M16[k]) * std::ldexp(1.0, 16 * (k - nl16 + 1));
-      cc.inv_Mest = static_cast<float>(1.0 / mest);
+      {
+        const int nl = crt_limbs(s);
+        double md = 0.0;
+        for (int k = kLimbs - 1; k >= 0; --k) md = md * 4294967296.0 + static_cast<double>(M.l[k]);
+        cc.inv_Ms = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / md);
+        // limb 0 (< 2^46) moves Y / M by less than 2^-49 once M > 2^95 (four or more limbs)
+        cc.est_lo = nl <= 3 ? 0 : 1;
+      }
       // byte limbs of M/m_t, four channels per word
       for (int t = 0; t < s; ++t) {
         Big Mt = M;

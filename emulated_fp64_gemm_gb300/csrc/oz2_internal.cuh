@@ -47,11 +47,10 @@ constexpr int kLimbs16 = 2 * kLimbs;  // 16-bit limbs of the same 160 bits
 struct CrtConsts {  // per-s CRT constants
   int s;
   int m[kSMax];
-  uint32_t Mt16[kSMax][kLimbs16]; // M/m_t in 16-bit limbs (one u32 each)
-  uint32_t M16[kLimbs16];         // M in 16-bit limbs
   uint32_t M[kLimbs];             // M, 32-bit limbs
   uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
-  float inv_Mest;                 // 1 / sum_l M16[l] 2^(16(l - NL16 + 1)) over the top six limbs, NL16 = 2 crt_limbs(s)
+  float inv_Ms;                   // 2^(32 (NL - 1)) / M, NL = crt_limbs(s)
+  int est_lo;                     // lowest 32-bit limb of Y the estimate of Y / M uses
   uint32_t L4[kSMax / 4][2 * kLimbs16];  // byte b of M/m_t for channels t = 4g .. 4g + 3, packed (dp4a); zero past s
 };
 
