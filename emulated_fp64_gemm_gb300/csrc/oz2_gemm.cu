@@ -44,6 +44,12 @@ namespace {
 constexpr int BM = 128;           // tile rows (TMEM lanes)
 constexpr int BK = 64;            // K per stage: 64 fp16 = one 128-byte swizzle row
 constexpr int KC_BLOCKS = 15;     // K-chunk = 15 * 64 = 960 terms (< 2^24 / 2^14 - margin)
+// Odd moduli (every channel but the first, m = 256): centered residues are at
+// most 127 in magnitude, so products are at most 127^2 = 16129 and a chunk of
+// 16 * 64 = 1024 terms on top of a reduced accumulator (|D| <= 127) stays an
+// exact fp32 integer: 127 + 1024 * 16129 = 16516223 < 2^24.  The modular GEMMs
+// of those channels reduce once every 1024 terms instead of every 960.
+constexpr int KC_BLOCKS_ODD = 16;
 constexpr int NUM_THREADS = 192;  // 6 warps
 constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
 
@@ -64,7 +70,8 @@ struct KParams {
   int64_t col0;     // first output column (and row of B's planes) of this launch (CTA-pair kernel)
   int s;
   int nkb;          // K blocks (qp / 64)
-  int nchunks;      // ceil(nkb / KC_BLOCKS)
+  int nchunks;      // ceil(nkb / KC_BLOCKS): channel 0, and every channel of the checking and bound GEMMs
+  int nchunks_odd;  // ceil(nkb / KC_BLOCKS_ODD): channels t >= 1 of the modular GEMMs
   int tiles_m, tiles_n, pairs_n;
   int64_t units;    // s * tiles_m * pairs_n
   uint8_t* R;
@@ -228,10 +235,15 @@ __device__ __forceinline__ void bound_final_keys2(uint32_t sum_addr, int64_t il,
     atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), (static_cast<unsigned long long>(rhi) << 32) | rlo);
 }
 
-// First K block of chunk c: the nkb blocks are split into nchunks chunks of
-// equal size (+-1), each at most KC_BLOCKS long.
-__device__ __forceinline__ int chunk_begin(int c, const KParams& kp) {
-  return static_cast<int>((static_cast<int64_t>(c) * kp.nkb) / kp.nchunks);
+// K-chunks of a unit of channel t.
+__device__ __forceinline__ int unit_nchunks(int t, const KParams& kp) {
+  return t == 0 ? kp.nchunks : kp.nchunks_odd;
+}
+
+// First K block of chunk c: the nkb blocks are split into nch chunks of equal
+// size (+-1), each at most KC_BLOCKS (channel 0) or KC_BLOCKS_ODD long.
+__device__ __forceinline__ int chunk_begin(int c, int nch, const KParams& kp) {
+  return static_cast<int>((static_cast<int64_t>(c) * kp.nkb) / nch);
 }
 
 // Final epilogue of one 32-column block: from 32 fp32 accumulators D (exact
@@ -343,9 +355,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
         const Unit U = decode_unit(u, kp);
-        for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = chunk_begin(c, kp);
-          const int kb1 = chunk_begin(c + 1, kp);
+        const int nch = unit_nchunks(U.t, kp);
+        for (int c = 0; c < nch && ok; ++c) {
+          const int kb0 = chunk_begin(c, nch, kp);
+          const int kb1 = chunk_begin(c + 1, nch, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             for (int kb = kb0; kb < kb1; ++kb) {
               if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs)) {
@@ -384,9 +397,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int64_t u = blockIdx.x; u < kp.units && ok; u += gridDim.x) {
         const Unit U = decode_unit(u, kp);
-        for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = chunk_begin(c, kp);
-          const int kb1 = chunk_begin(c + 1, kp);
+        const int nch = unit_nchunks(U.t, kp);
+        for (int c = 0; c < nch && ok; ++c) {
+          const int kb0 = chunk_begin(c, nch, kp);
+          const int kb1 = chunk_begin(c + 1, nch, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             if (!mbar_wait_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               ok = false;
@@ -442,8 +456,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float mf = kp.mf[U.t];
       const float inv_m = kp.inv_mf[U.t];
       const float wm = kp.wmul[U.t];
-      for (int c = 0; c < kp.nchunks && ok; ++c) {
-        const bool last = (c == kp.nchunks - 1);
+      const int nch = unit_nchunks(U.t, kp);
+      for (int c = 0; c < nch && ok; ++c) {
+        const bool last = (c == nch - 1);
         for (int sl = 0; sl < U.ntile; ++sl) {
           // every lane waits; the outcome is made warp-uniform so the
           // .sync.aligned TMEM accesses below stay convergent
@@ -763,9 +778,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
       for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
         const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
         const int arow = static_cast<int>(kp.row0) + U.mp * 256 + static_cast<int>(rank) * 128;
-        for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = chunk_begin(c, kp);
-          const int kb1 = chunk_begin(c + 1, kp);
+        const int nch = unit_nchunks(U.t, kp);
+        for (int c = 0; c < nch && ok; ++c) {
+          const int kb0 = chunk_begin(c, nch, kp);
+          const int kb1 = chunk_begin(c + 1, nch, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             const int brow = static_cast<int>(kp.col0) + (U.tn0 + sl) * BN + static_cast<int>(rank) * (BN / 2);
             for (int kb = kb0; kb < kb1; ++kb) {
@@ -803,9 +819,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
       bool ok = true;
       for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
         const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
-        for (int c = 0; c < kp.nchunks && ok; ++c) {
-          const int kb0 = chunk_begin(c, kp);
-          const int kb1 = chunk_begin(c + 1, kp);
+        const int nch = unit_nchunks(U.t, kp);
+        for (int c = 0; c < nch && ok; ++c) {
+          const int kb0 = chunk_begin(c, nch, kp);
+          const int kb1 = chunk_begin(c + 1, nch, kp);
           for (int sl = 0; sl < U.ntile && ok; ++sl) {
             if (!mbar_wait_cluster_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               ok = false;
@@ -861,8 +878,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
       const float mf = kp.mf[U.t];
       const float inv_m = kp.inv_mf[U.t];
       const float wm = kp.wmul[U.t];
-      for (int c = 0; c < kp.nchunks && ok; ++c) {
-        const bool last = (c == kp.nchunks - 1);
+      const int nch = unit_nchunks(U.t, kp);
+      for (int c = 0; c < nch && ok; ++c) {
+        const bool last = (c == nch - 1);
         for (int sl = 0; sl < U.ntile; ++sl) {
           const bool got = mbar_wait_cluster_bounded(smem_u32(&accf[sl]), use[sl] & 1, abort_flag, kWaitLimitNs);
           if (!__all_sync(0xffffffffu, got)) {
@@ -984,6 +1002,7 @@ cudaError_t launch_impl(const GemmArgs& g, const ModConsts& mc, cudaStream_t st)
   kp.s = g.s;
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
+  kp.nchunks_odd = (KIND == kGemmMod) ? (kp.nkb + KC_BLOCKS_ODD - 1) / KC_BLOCKS_ODD : kp.nchunks;
   kp.tiles_m = static_cast<int>((g.p + BM - 1) / BM);
   kp.col0 = g.col0;
   kp.tiles_n = static_cast<int>(((g.ncols ? g.ncols : g.r) + BN - 1) / BN);
@@ -1026,6 +1045,7 @@ cudaError_t launch_2sm(const GemmArgs& g, const ModConsts& mc, cudaStream_t st) 
   kp.s = g.s;
   kp.nkb = static_cast<int>(g.qp / BK);
   kp.nchunks = (kp.nkb + KC_BLOCKS - 1) / KC_BLOCKS;
+  kp.nchunks_odd = (KIND == kGemmMod) ? (kp.nkb + KC_BLOCKS_ODD - 1) / KC_BLOCKS_ODD : kp.nchunks;
   kp.tiles_m = static_cast<int>((g.p + 255) / 256);  // 256-row pair tiles
   kp.col0 = g.col0;
   const int64_t ncols = g.ncols ? g.ncols : g.r;
