@@ -8,7 +8,7 @@
 // tcgen05.mma.kind::f16 into fp32 accumulators in tensor memory.  Every
 // product is an integer of magnitude <= 2^14 and every partial sum stays an
 // integer below 2^24 in magnitude, so the fp32 accumulation is exact as long
-// as a K-chunk holds at most 960 terms:
+// as a K-chunk holds at most 960 terms (1024 for the odd moduli, below):
 //   * kGemmMod (the production path): after each K-chunk the epilogue warps
 //     replace every accumulator D by D - m*rint(D/m), an exact fp32
 //     operation leaving |D| <= 129, and the next chunk accumulates on top.

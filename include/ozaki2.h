@@ -43,7 +43,7 @@
  * dimension within its mode's limit below.  The INT32 condition q < 131072
  * of "Ozaki II supplement: INT8 range conditions and paper performance
  * results" §1.3 bounds one unblocked accumulation; the modular GEMMs here
- * reduce every K-block of at most 960 terms modulo m_t before the next is
+ * reduce every K-block of at most 960 terms (1024 for odd m_t) modulo m_t before the next is
  * added (the blocking that section describes for larger q), so the result
  * R_t = P_t mod m_t is exact for any q.  What remains: the fast-mode
  * sum-of-squares statistic is a 64-bit sum of q terms below 2^40
