@@ -15,20 +15,20 @@
  *   results" (cited [S]) §1.1 pipeline, §1.2 centered residues, §1.3 the
  *   INT32 condition, §2 Eq. (18).
  *   O0  moduli: walk down from 256, keep each integer coprime to every one
- *       kept (reading R1); M = prod m_t, L = M/2 - 1 (R2).
- *   O2  exponents.  fast (R5): e = floor(log2 max|x|) + 1,
+ *       kept; M = prod m_t, L = M/2 - 1.
+ *   O2  exponents.  fast: e = floor(log2 max|x|) + 1,
  *       S = sum ceil(|x| 2^(20 - e))^2 (exact), alpha = max {a : 4^a S 4^(e-20) <= L}.
- *       accu (R6): u = max {u : ceil(max|x| 2^u) <= 127}, Abar = ceil(|A| 2^u),
+ *       accu: u = max {u : ceil(max|x| 2^u) <= 127}, Abar = ceil(|A| 2^u),
  *       Bbar likewise with v, Wbar = Abar Bbar (exact), U_i = max_j Wbar_ij 2^-(u_i+v_j),
  *       V_j = max_i (same), alpha_i = max {a : 4^a U_i <= L}, beta_j likewise.
- *   O3  A' = trunc(2^alpha A), B' = trunc(B 2^beta), toward zero (R7).
+ *   O3  A' = trunc(2^alpha A), B' = trunc(B 2^beta), toward zero.
  *   O4  rho_m(x) = ((x + floor(m/2)) mod m) - floor(m/2) for every modulus.
  *   O5  P_t = A_t B_t exactly (64-bit sums).
- *   O6  R_t = P_t mod m_t in [0, m_t) (R8).
+ *   O6  R_t = P_t mod m_t in [0, m_t).
  *   O7  w_t = R_t (M/m_t)^-1 mod m_t, Y = sum w_t M/m_t mod M,
- *       X = Y - M if 2Y >= M else Y, so X in [-M/2, M/2) (R9).
+ *       X = Y - M if 2Y >= M else Y, so X in [-M/2, M/2).
  *   O8  C = RN_even(X 2^-(alpha_i + beta_j)), one correct rounding, with
- *       subnormals and overflow to +-Inf (R10).
+ *       subnormals and overflow to +-Inf.
  * All integer stages are exact: multiword integers of 32-bit limbs, 64- and
  * 128-bit sums.  The only arrangement beyond the definition is in the
  * integer matrix products, which are evaluated over blocks of rows, columns
@@ -63,8 +63,8 @@
 #include <string.h>
 
 #define SMAX 20
-#define FBITS 20   /* fractional bits of the fast statistic (R5) */
-#define QMAX8 127  /* largest upward-quantised bound entry (R6) */
+#define FBITS 20   /* fractional bits of the fast statistic */
+#define QMAX8 127  /* largest upward-quantised bound entry */
 #define NW 8       /* 32-bit limbs of a multiword integer: 256 bits */
 
 /* ------------------------------------------------------------------ multiword */
@@ -390,7 +390,7 @@ static double vec_elem(const expctx* x, int side, int64_t k, int64_t l) {
   return side == 0 ? x->A[l * x->lda + k] : x->B[k * x->ldb + l];
 }
 
-/* fast bound ([P] §2, §5.1; R5) for one vector */
+/* fast bound ([P] §2, §5.1) for one vector */
 static int32_t fast_exponent(const expctx* x, int side, int64_t k) {
   double amax = 0.0;
   for (int64_t l = 0; l < x->q; ++l) {
@@ -421,7 +421,7 @@ static void fast_task(void* ctx, int64_t task) {
   else x->beta[task - x->p] = fast_exponent(x, 1, task - x->p);
 }
 
-/* R6: u = max {u : ceil(amax 2^u) <= 127}, 0 for a zero vector */
+/* u = max {u : ceil(amax 2^u) <= 127}, 0 for a zero vector */
 static int32_t quant_exponent(double amax) {
   if (amax == 0.0) return 0;
   int neg, E;

@@ -36,19 +36,19 @@ from fractions import Fraction
 import numpy as np
 
 # Fractional bits kept per element in the fast-mode sum-of-squares statistic
-# (reading R5).  Each rounded-up term is <= 2**F and its square <= 2**(2F),
+# (each |x| is rounded up to a multiple of 2**(e - F)).  Each rounded-up term is <= 2**F and its square <= 2**(2F),
 # so for q < 2**24 the sum of squares is < 2**64 and fits an unsigned 64-bit
 # integer (FAST_Q_LIMIT); it is summed in uint64, since from q = 2**23 on it
 # can pass 2**63.
 F_FAST = 20
-# Largest magnitude of an upward-quantised bound entry: signed INT8 (reading R6).
+# Largest magnitude of an upward-quantised bound entry: signed INT8.
 BOUND_QMAX = 127
 # [S] §1.3: q * 2**14 < 2**31  <=>  q < 131072, the bound for one unblocked
 # INT32 accumulation of a residue product.  For longer inner dimensions the
 # same section splits K into blocks, reduces each block's product modulo the
 # modulus and combines the residues; the result R_t = P_t mod m_t is the same
 # number, so the oracle computes P_t exactly (int64: |P_t| <= q 2**14) and
-# reduces it, for any q (reading R14).
+# reduces it, for any q.
 Q_LIMIT = 131072
 # Limits that remain: the 64-bit fast statistic (above) and the accu bound
 # product Wbar = Abar Bbar, an exact INT32 accumulation (q 127**2 < 2**31).
@@ -60,7 +60,7 @@ ACCU_Q_LIMIT = 133145
 # O0  moduli and CRT constants
 # ----------------------------------------------------------------------------
 def greedy_moduli(s: int) -> list[int]:
-    """R1: walk down from 256, keep each integer coprime to every one kept.
+    """Walk down from 256, keep each integer coprime to every one kept.
 
     [S] §1.2 asks only for pairwise-coprime m_t <= 256, with larger moduli
     giving more range bits; taking them greedily from the top is the plainest
@@ -82,7 +82,7 @@ def greedy_moduli(s: int) -> list[int]:
 def modulus_constants(moduli: list[int]) -> dict:
     """M = prod m_t, the CRT weights M/m_t and their inverses mod m_t.
 
-    R2: the reconstruction bound is L = M/2 - 1 (Eq. (18)'s numerator in [S] §2;
+    The reconstruction bound is L = M/2 - 1 (Eq. (18)'s numerator in [S] §2;
     [P] §1 asks max |(A'B')_ij| < M/2).
     """
     M = 1
@@ -129,7 +129,7 @@ def ceil_scaled(mant: np.ndarray, E: np.ndarray, k) -> np.ndarray:
 
 
 def max_pow4_exponent(U: Fraction, L: int) -> int:
-    """max { a in Z : 4**a * U <= L }, and 0 when U == 0 (reading R4)."""
+    """max { a in Z : 4**a * U <= L }, and 0 when U == 0 (an all-zero vector leaves a free)."""
     if U < 0:
         raise ValueError("a bound on a sum of squares or of |A||B| cannot be negative")
     if U == 0:
@@ -156,7 +156,7 @@ def fast_exponents(X: np.ndarray, axis: int, L: int) -> np.ndarray:
 
     For each vector x (a row of A: axis=1; a column of B: axis=0):
       e   = floor(log2 max|x|) + 1,
-      S   = sum_l ceil(|x_l| * 2**(F - e))**2   (an exact integer: R5),
+      S   = sum_l ceil(|x_l| * 2**(F - e))**2   (an exact integer),
       U   = S * 2**(2(e - F))  >=  ||x||_2**2,
       exp = max { a : 4**a * U <= L }.
     By Cauchy-Schwarz (|A||B|)_ij <= ||A(i,:)|| ||B(:,j)||, so the scaled
@@ -186,7 +186,7 @@ def fast_exponents(X: np.ndarray, axis: int, L: int) -> np.ndarray:
 
 
 def bound_quant_exponents(amax: np.ndarray) -> np.ndarray:
-    """R6: u = max { u : ceil(amax * 2**u) <= 127 } (0 for a zero vector)."""
+    """u = max { u : ceil(amax * 2**u) <= 127 } (0 for a zero vector)."""
     out = np.zeros(amax.shape, dtype=np.int64)
     for i, a in enumerate(np.asarray(amax, dtype=np.float64)):
         if a == 0.0:
@@ -263,8 +263,8 @@ def accu_exponents(A: np.ndarray, B: np.ndarray, L: int):
 
     Abar = ceil(|A| * 2**u_i) (rows), Bbar = ceil(|B| * 2**v_j) (columns),
     Wbar = Abar Bbar (exact), W_ij = Wbar_ij * 2**(-u_i - v_j) >= (|A||B|)_ij.
-    R6 (reading of "row/column maxima of the bound output -> final scale
-    exponents"): U_i = max_j W_ij, V_j = max_i W_ij,
+    Reading of "row/column maxima of the bound output -> final scale
+    exponents" as a geometric-mean split: U_i = max_j W_ij, V_j = max_i W_ij,
       alpha_i = max { a : 4**a U_i <= L },  beta_j = max { b : 4**b V_j <= L }.
     Then 2**(alpha_i + beta_j) W_ij <= sqrt(4**alpha_i U_i * 4**beta_j V_j) <= L.
     Returns (alpha, beta, Abar, Bbar, u, v, Wbar).
@@ -302,7 +302,7 @@ def centered_residue(x, m: int):
 
 
 def scaled_trunc_bigint(x: float, k: int) -> int:
-    """trunc(2**k * x) as a Python integer (R7: truncation toward zero, [P] §1)."""
+    """trunc(2**k * x) as a Python integer (truncation toward zero, [P] §1)."""
     if x == 0.0:
         return 0
     fx = Fraction(float(x)) * Fraction(2) ** k
@@ -356,7 +356,7 @@ def products(Ares: np.ndarray, Bres: np.ndarray) -> np.ndarray:
 
 
 def output_residues(P: np.ndarray, moduli: list[int]) -> np.ndarray:
-    """R_t = P_t mod m_t, nonnegative ([P] §1 blue stage; reading R8)."""
+    """R_t = P_t mod m_t, nonnegative ([P] §1 blue stage; the nonnegative remainder)."""
     R = np.empty(P.shape, dtype=np.int64)
     for t, m in enumerate(moduli):
         R[t] = np.mod(P[t], m)
@@ -367,7 +367,7 @@ def crt(residues, consts: dict) -> int:
     """CRT_M: the unique X in [-M/2, M/2) with X = R_t (mod m_t) for all t.
 
     [P] §1 red stage.  w_t = R_t * inv_t mod m_t, Y = sum_t w_t M/m_t mod M,
-    X = Y - M if Y >= M/2 else Y (reading R9: -M/2 included, M/2 excluded).
+    X = Y - M if Y >= M/2 else Y (-M/2 included, M/2 excluded).
     """
     M = consts["M"]
     Y = 0
@@ -393,7 +393,7 @@ def round_scaled(X: int, k: int) -> float:
     """RN_even(X * 2**-k): one correct rounding to double, with overflow to +-inf.
 
     Python's int true division and int-to-float conversion are correctly
-    rounded (ties to even), subnormal range included (reading R10).
+    rounded (ties to even), subnormal range included.
     """
     X = int(X)
     if X == 0:

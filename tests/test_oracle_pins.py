@@ -308,7 +308,7 @@ def _max_pow4_brute(U: Fraction, L: int) -> int:
 
 @pytest.mark.parametrize("q", [1 << 23, (1 << 23) + 1])
 def test_fast_statistic_past_two_to_the_63(q):
-    """[P] §5.1 (sum of squares rounded up), reading R5 at the top of its range.
+    """[P] §5.1 (sum of squares rounded up) at the top of its range.
 
     Every entry is 1 - 2**-53, the largest double below 1: e = 0 and every
     rounded-up term is ceil((1 - 2**-53) 2**20) = 2**20, so S = q 2**40 >= 2**63

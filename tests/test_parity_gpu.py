@@ -429,3 +429,41 @@ def test_workspace_release_and_recreate(oz2):
     ref = oracle.oracle_entries(A, B, 14, "fast", np.arange(0, 2500, 97), np.arange(0, 2000, 79)[:26])
     assert ulp_distance(C2[np.arange(0, 2500, 97), np.arange(0, 2000, 79)[:26]], ref["C"]) <= ULP_TOL
     assert oz2.last_error() == 0
+
+
+@pytest.mark.parametrize("s", [2, 8, 14, 18])
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_crt_at_the_edge_of_its_range(oz2, s, sign):
+    """X next to +-M/2, where the CRT's quotient estimate can round to the
+    wrong side and the exact comparison with M/2 must correct it.
+
+    A is a row of q ones and B a column of q (+-)ones.  The fast bound of
+    "Profiling Ozaki II: The Cost Behind Fast INT8 GEMMs" §5.1 sees e = 1 and
+    q terms ceil(1 * 2^19)^2, so U = q and alpha = beta = a with
+    a = max {a : 4^a q <= L}.  With q = floor(L / 4^a0) the product
+    X = A'B' = +-q 4^a (§1) lies within 4^a of L = M/2 - 1, about M/(2q)
+    below M/2, closer than the float estimate of X/M resolves; C = +-q."""
+    ms = oracle.greedy_moduli(s)
+    M = 1
+    for m in ms:
+        M *= m
+    L = M // 2 - 1
+    a0 = 0
+    while L // 4 ** (a0 + 1) >= 1 and L // 4 ** a0 >= 2**23:
+        a0 += 1
+    q = L // 4**a0
+    a = 0
+    while 4 ** (a + 1) * q <= L:
+        a += 1
+    assert a == a0 and 0 < L - q * 4**a < 4**a
+    A = np.ones((1, q))
+    B = np.full((q, 1), sign)
+    got = oz2.dgemm_debug(_dev(A), _dev(B), s, "fast", want_p=False)
+    torch.cuda.synchronize()
+    assert got["alpha"].cpu().numpy()[0] == a and got["beta"].cpu().numpy()[0] == a
+    x = decode_x(got["X"].cpu().numpy()[0, 0])
+    assert x == int(sign) * q * 4**a
+    assert got["C"].cpu().numpy()[0, 0] == sign * q
+    C = oz2.dgemm(_dev(A), _dev(B), s, "fast").cpu().numpy()
+    assert C[0, 0] == sign * q
+    assert oz2.last_error() == 0
