@@ -112,12 +112,31 @@ def moduli(s: int) -> list[int]:
 
 
 def _colmajor(T):
-    """(ptr, ld) if T (2-D) is column-major with ld >= rows, else None."""
+    """(ptr, ld) if T (2-D) is column-major with ld >= rows, else None.
+
+    The stride of a dimension of size 1 is never used to address an element,
+    so it is not checked: a 1 x q row with any row stride and a p x 1 column
+    with any column stride are column-major."""
     p, q = T.shape
     s0, s1 = T.stride()
-    if s0 == 1 and (s1 >= max(p, 1) or q == 1):
-        return T.data_ptr(), max(s1, p)
-    return None
+    if p > 1 and s0 != 1:
+        return None
+    if q <= 1:
+        return T.data_ptr(), max(p, 1)
+    if s1 < max(p, 1):
+        return None
+    return T.data_ptr(), s1
+
+
+def _as_colmajor(T):
+    """T itself if column-major, else a column-major copy."""
+    import torch
+
+    if _colmajor(T) is not None:
+        return T
+    C = torch.empty((T.shape[1], T.shape[0]), dtype=T.dtype, device=T.device).t()
+    C.copy_(T)
+    return C
 
 
 def _stream_handle(stream):
@@ -136,15 +155,8 @@ def _prepare(A, B):
         raise ValueError("A and B must be CUDA tensors on the same device")
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}")
-    a = _colmajor(A)
-    b = _colmajor(B)
-    if a is None:
-        A = A.t().contiguous().t()
-        a = _colmajor(A)
-    if b is None:
-        B = B.t().contiguous().t()
-        b = _colmajor(B)
-    return A, B, a, b
+    A, B = _as_colmajor(A), _as_colmajor(B)
+    return A, B, _colmajor(A), _colmajor(B)
 
 
 def dgemm(A, B, s: int = 14, mode="fast", out=None, stream=None):
@@ -226,13 +238,8 @@ def dgemm_host(A, B, s: int = 14, mode="fast", out=None, stream=None):
         raise ValueError("dgemm_host takes host (CPU) tensors")
     if A.dtype != torch.float64 or B.dtype != torch.float64:
         raise TypeError("A and B must be float64")
+    A, B = _as_colmajor(A), _as_colmajor(B)
     a, b = _colmajor(A), _colmajor(B)
-    if a is None:
-        A = A.t().contiguous().t()
-        a = _colmajor(A)
-    if b is None:
-        B = B.t().contiguous().t()
-        b = _colmajor(B)
     p, q = A.shape
     r = B.shape[1]
     if out is None:

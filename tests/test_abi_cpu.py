@@ -81,3 +81,34 @@ def test_no_gpu_means_a_loud_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _call(lib) == 4  # OZ2_ERR_CUDA: there is no CPU fallback
+
+
+def test_column_major_views_pass_through_and_others_are_copied():
+    """The binding hands the library (pointer, leading dimension) of a
+    column-major view as it is and copies anything else into one."""
+    torch = pytest.importorskip("torch")
+    base = torch.arange(60, dtype=torch.float64).reshape(6, 10)  # row-major
+    cases = [
+        base.t(),                       # 10 x 6 column-major, ld 10
+        base.t()[2:7, 1:4],             # a block of it, ld 10
+        base[2:3, :],                   # 1 x 10 row, row stride 10
+        base.t()[:, 4:5],               # 10 x 1 column, column stride 10
+        torch.ones(1, 7, dtype=torch.float64).as_strided((1, 7), (7, 1)),
+        torch.ones(7, 1, dtype=torch.float64).as_strided((7, 1), (1, 1)),
+        torch.ones(1, 1, dtype=torch.float64),
+    ]
+    for T in cases:
+        ptr, ld = oz2._colmajor(T)
+        assert ptr == T.data_ptr() and ld >= T.shape[0]
+        assert oz2._as_colmajor(T) is T
+        # every element sits at ptr + 8 (i + j ld)
+        flat = T.untyped_storage()
+        for i in range(T.shape[0]):
+            for j in range(T.shape[1]):
+                off = (ptr - T.untyped_storage().data_ptr()) // 8 + i + j * ld
+                assert torch.tensor([], dtype=torch.float64).set_(flat)[off] == T[i, j]
+    for T in [base, base[:, 1:3], base[:, 4:5], torch.ones(3, 4, dtype=torch.float64).expand(3, 4)[:, :],
+              torch.ones(1, 4, dtype=torch.float64).expand(3, 4)]:
+        assert oz2._colmajor(T) is None
+        C = oz2._as_colmajor(T)
+        assert oz2._colmajor(C) is not None and torch.equal(C, T)
