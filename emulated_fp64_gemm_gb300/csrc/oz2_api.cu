@@ -155,13 +155,11 @@ const Tables& tables() {
       Big Mh = M;
       big_divmod_small(Mh, 2);
       for (int k = 0; k < kLimbs; ++k) cc.Mhalf[k] = Mh.l[k];
+      for (int q = 0; q < kLimbs16; ++q) cc.M16[q] = (M.l[q / 2] >> (16 * (q % 2))) & 0xFFFFu;
       {
-        const int nl = crt_limbs(s);
         double md = 0.0;
         for (int k = kLimbs - 1; k >= 0; --k) md = md * 4294967296.0 + static_cast<double>(M.l[k]);
-        cc.inv_Ms = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / md);
-        // limb 0 (< 2^46) moves Y / M by less than 2^-49 once M > 2^95 (four or more limbs)
-        cc.est_lo = nl <= 3 ? 0 : 1;
+        for (int b = 0; b < 2 * kLimbs16; ++b) cc.est_f[b] = static_cast<float>(std::ldexp(1.0, 8 * b) / md);
       }
       // byte limbs of M/m_t, four channels per word
       for (int t = 0; t < s; ++t) {

@@ -9,17 +9,23 @@
 // (bytes), so here
 //   Y = sum_t w_t (M/m_t)
 // is accumulated as byte-limb sums S_b = sum_t w_t byte_b(M/m_t) with dp4a,
-// four channels per instruction (each S_b < 2^20), and gathered into NL
-// unnormalised 32-bit limbs (each < 2^46).  A float estimate of Y / M gives
-// k = round(Y / M), and X = Y - k M follows with exact 64-bit carries.
-// Because |X| <= M/2 - 1 always (the scaling bound of the method), X is in
-// range unless Y / M lies within the estimate's error (far below 2^-12) of a
+// four channels per instruction (each S_b < 2^20).  k = round(Y / M) comes
+// from a float sum of the top byte-limb sums weighted by 2^(8b) / M, and
+// X = Y - k M is carried through 16-bit limbs in 32-bit arithmetic.  Because
+// |X| <= M/2 - 1 always (the scaling bound of the method), X is in range
+// unless Y / M lies within the estimate's error (far below 2^-12) of a
 // half-integer; only then is X compared with M/2 exactly and moved by M.
-// The rounding takes the top 64 bits of |X| with a sticky bit for the rest,
-// converts them once with the correctly rounded u64 -> double conversion
-// (the sticky bit sits 10 bits below the rounding position, so the result is
-// RN of |X| itself) and scales by adding to the exponent field; a subnormal or
+// The rounding takes a signed 64-bit window of X (sign bit, then the first
+// bit that differs from it) with a sticky bit for the rest, converts it once
+// with the correctly rounded signed 64-bit -> double conversion (the sticky
+// bit sits 9 bits below the rounding position, so the result is RN of X
+// itself) and scales by adding to the exponent field; a subnormal or
 // overflowing result takes an exact integer rounding path instead.
+//
+// The device's FP64 pipe also executes every 64-bit integer <-> floating
+// conversion and runs at a small fraction of the other pipes' rate, so the
+// kernel keeps to one such conversion per output; the quotient estimate uses
+// 32-bit conversions only.
 #include <algorithm>
 
 #include "oz2_internal.cuh"
@@ -27,55 +33,46 @@
 namespace oz2 {
 namespace {
 
-// RN_even(X 2^-k) for X in NL 32-bit two's complement words, by exact integer
-// rounding of the top 64 bits of |X| with a sticky bit for the rest: the path
-// for results that are subnormal or overflow.
+__device__ __forceinline__ uint64_t pack64(uint32_t hi, uint32_t lo) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// RN_even(X 2^-k) for X in NL 32-bit two's complement words (x0 lowest; the
+// words past NL are ignored), by exact integer rounding of the top 64 bits of
+// |X| with a sticky bit for the rest: the path for results that are subnormal
+// or overflow.  Out of line, with the words in registers.
 template <int NL>
-__device__ __forceinline__ double round_x_exact(const uint32_t (&x)[NL], int k) {
-  const bool neg = static_cast<int32_t>(x[NL - 1]) < 0;
-  uint32_t mg[NL + 1];
+__device__ __noinline__ double round_x_exact(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3,
+                                             uint32_t x4, int k) {
+  const uint32_t xin[5] = {x0, x1, x2, x3, x4};
+  const bool neg = static_cast<int32_t>(xin[NL - 1]) < 0;
+  uint32_t mg[6] = {0, 0, 0, 0, 0, 0};
   {
     uint64_t c = neg ? 1u : 0u;
 #pragma unroll
     for (int j = 0; j < NL; ++j) {
-      const uint64_t t = static_cast<uint64_t>(neg ? ~x[j] : x[j]) + c;
+      const uint64_t t = static_cast<uint64_t>(neg ? ~xin[j] : xin[j]) + c;
       mg[j] = static_cast<uint32_t>(t);
       c = t >> 32;
     }
-    mg[NL] = 0;
   }
-  constexpr int NW = (NL + 1) / 2;
-  uint64_t W[NW];
-#pragma unroll
-  for (int w = 0; w < NW; ++w) W[w] = static_cast<uint64_t>(mg[2 * w]) | (static_cast<uint64_t>(mg[2 * w + 1]) << 32);
+  const uint64_t W0 = pack64(mg[1], mg[0]), W1 = pack64(mg[3], mg[2]), W2 = pack64(mg[5], mg[4]);
   uint64_t hi, lo;
   bool st = false;
   int base;
-  if (NW == 3) {
-    if (W[2]) {
-      hi = W[2];
-      lo = W[1];
-      st = W[0] != 0;
-      base = 128;
-    } else if (W[1]) {
-      hi = W[1];
-      lo = W[0];
-      base = 64;
-    } else {
-      hi = W[0];
-      lo = 0;
-      base = 0;
-    }
+  if (W2) {
+    hi = W2;
+    lo = W1;
+    st = W0 != 0;
+    base = 128;
+  } else if (W1) {
+    hi = W1;
+    lo = W0;
+    base = 64;
   } else {
-    if (W[NW - 1]) {
-      hi = W[NW - 1];
-      lo = W[0];
-      base = 64;
-    } else {
-      hi = W[0];
-      lo = 0;
-      base = 0;
-    }
+    hi = W0;
+    lo = 0;
+    base = 0;
   }
   if (hi == 0) return 0.0;
   const int lz = __clzll(static_cast<long long>(hi));
@@ -111,87 +108,79 @@ __device__ __forceinline__ double round_x_exact(const uint32_t (&x)[NL], int k) 
   return __longlong_as_double(static_cast<long long>(bits));
 }
 
-// C = RN_even(X 2^-k) for X in NL 32-bit two's complement words.
+// C = RN_even(X 2^-k) for X in NL 32-bit two's complement words.  T is a
+// signed 64-bit window of X whose top bit is the sign and whose next bit is
+// the first that differs from it (or all of X when it fits in 64 bits), so
+// X = (T + f) 2^sh with 0 <= f < 1.  Setting bit 0 of T when f > 0 leaves the
+// rounding unchanged: the rounding position of |T| >= 2^62 is bit 10, and an
+// odd value 9 bits below it is never a tie nor across one from T + f.
 template <int NL>
 __device__ __forceinline__ double round_x(const uint32_t (&x)[NL], int k) {
-  const bool neg = static_cast<int32_t>(x[NL - 1]) < 0;
-  uint32_t mg[NL + 1];
-  {
-    uint64_t c = neg ? 1u : 0u;
-#pragma unroll
-    for (int j = 0; j < NL; ++j) {
-      const uint64_t t = static_cast<uint64_t>(neg ? ~x[j] : x[j]) + c;
-      mg[j] = static_cast<uint32_t>(t);
-      c = t >> 32;
-    }
-    mg[NL] = 0;
-  }
-  constexpr int NW = (NL + 1) / 2;
-  uint64_t W[NW];
-#pragma unroll
-  for (int w = 0; w < NW; ++w) W[w] = static_cast<uint64_t>(mg[2 * w]) | (static_cast<uint64_t>(mg[2 * w + 1]) << 32);
-  uint64_t hi, lo;
+  int64_t H;
+  uint64_t L;
   bool st = false;
-  int base;
-  if (NW == 3) {
-    if (W[2]) {
-      hi = W[2];
-      lo = W[1];
-      st = W[0] != 0;
-      base = 128;
-    } else if (W[1]) {
-      hi = W[1];
-      lo = W[0];
-      base = 64;
-    } else {
-      hi = W[0];
-      lo = 0;
-      base = 0;
-    }
+  int base = 64;
+  if constexpr (NL == 3) {
+    H = static_cast<int32_t>(x[2]);
+    L = pack64(x[1], x[0]);
+  } else if constexpr (NL == 4) {
+    H = static_cast<int64_t>(pack64(x[3], x[2]));
+    L = pack64(x[1], x[0]);
   } else {
-    if (W[NW - 1]) {
-      hi = W[NW - 1];
-      lo = W[0];
-      base = 64;
+    static_assert(NL == 5, "three to five words");
+    const int64_t H2 = static_cast<int32_t>(x[4]);
+    const uint64_t M1 = pack64(x[3], x[2]);
+    const uint64_t L0 = pack64(x[1], x[0]);
+    if (H2 != (static_cast<int64_t>(M1) >> 63)) {  // X needs the top word
+      H = H2;
+      L = M1;
+      st = L0 != 0;
+      base = 128;
     } else {
-      hi = W[0];
-      lo = 0;
-      base = 0;
+      H = static_cast<int64_t>(M1);
+      L = L0;
     }
   }
-  if (hi == 0) return 0.0;  // X == 0
-  const int lz = __clzll(static_cast<long long>(hi));
-  const uint64_t T = lz ? ((hi << lz) | (lo >> (64 - lz))) : hi;  // top 64 bits of |X|, MSB at bit 63
-  st = st || ((lo << lz) != 0);
-  // |X| = (T + f) 2^(base - lz) with 0 <= f < 1
-  const uint64_t db = static_cast<uint64_t>(__double_as_longlong(__ull2double_rn(T | (st ? 1ull : 0ull))));
-  const int sc = base - lz - k;
-  const int e = static_cast<int>(db >> 52) - 1023 + sc;  // unbiased exponent of the result
-  if (e >= -1022 && e <= 1023) {
-    uint64_t bits = db + (static_cast<uint64_t>(static_cast<int64_t>(sc)) << 52);
-    if (neg) bits |= 1ull << 63;
-    return __longlong_as_double(static_cast<long long>(bits));
+  int64_t T;
+  int sh;
+  if (H == (static_cast<int64_t>(L) >> 63)) {  // the window is L itself
+    T = static_cast<int64_t>(L);
+    sh = base - 64;
+    if (T == 0 && !st) return 0.0;
+  } else {
+    const int n = __clzll(H ^ (H >> 63)) - 1;  // redundant sign bits of H: 0 .. 63
+    T = n ? static_cast<int64_t>((static_cast<uint64_t>(H) << n) | (L >> (64 - n))) : H;
+    st = st || ((L << n) != 0);
+    sh = base - n;
   }
-  return round_x_exact<NL>(x, k);  // subnormal or overflowing result
+  const uint64_t db = static_cast<uint64_t>(__double_as_longlong(__ll2double_rn(T | (st ? 1ll : 0ll))));
+  const int sc = sh - k;
+  const int e = static_cast<int>((db >> 52) & 0x7FF) - 1023 + sc;  // unbiased exponent of the result
+  if (e >= -1022 && e <= 1023)
+    return __longlong_as_double(static_cast<long long>(db + (static_cast<uint64_t>(static_cast<int64_t>(sc)) << 52)));
+  return round_x_exact<NL>(x[0], x[1], x[2], NL > 3 ? x[NL > 3 ? 3 : 0] : 0u, NL > 4 ? x[NL > 4 ? 4 : 0] : 0u,
+                           k);  // subnormal or overflowing result
 }
 
 // Output rows [row0, row0 + rows).  W holds the coefficients as
 // [s][r4][p_total][4] (four consecutive columns of one row per word); X has
 // p_total rows per column.  Thread = (row i, group of 4 columns); x walks the
 // rows, y a strided set of column groups.  MAXS: the largest s the instance
-// serves; NL: 32-bit limbs of Y (crt_limbs); NBC: the byte limbs of the
-// largest M/m_t (s - 1 for s >= 5); the dp4a loop stops there.  Four blocks
-// per SM: the kernel is latency-bound (long dependent chains per output), so
-// occupancy pays even with a few spilled registers.
-template <int MAXS, int NL, int NBC>
-__global__ void __launch_bounds__(256, 4) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
-                                                     int64_t jg0, int64_t jg1, int64_t r,
-                                                     const __grid_constant__ CrtConsts cc,
-                                                     const uint8_t* __restrict__ Wb,
-                                                     const int32_t* __restrict__ alpha,
-                                                     const int32_t* __restrict__ beta,
-                                                     double* __restrict__ C, int64_t ldc,
-                                                     uint64_t* __restrict__ Xout) {
+// serves; NL: 32-bit words of Y (crt_limbs); NBC: the byte limbs of the
+// largest M/m_t (s - 1 for s >= 5), where the dp4a loop stops; EB0: the lowest
+// byte-limb sum the quotient estimate takes (below it the sums move Y / M by
+// less than 2^-36 for every s the instance serves); MINB: blocks per SM (the
+// kernel is issue-bound; four where the registers allow it without spills);
+// WX: also write X (checking path).
+template <int MAXS, int NL, int NBC, int EB0, int MINB, bool WX>
+__global__ void __launch_bounds__(256, MINB) crt_kernel(int64_t row0, int64_t rows, int64_t p_total,
+                                                        int64_t jg0, int64_t jg1, int64_t r,
+                                                        const __grid_constant__ CrtConsts cc,
+                                                        const uint8_t* __restrict__ Wb,
+                                                        const int32_t* __restrict__ alpha,
+                                                        const int32_t* __restrict__ beta,
+                                                        double* __restrict__ C, int64_t ldc,
+                                                        uint64_t* __restrict__ Xout) {
   const int64_t il = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (il >= rows) return;
   const int64_t i = row0 + il;
@@ -200,8 +189,8 @@ __global__ void __launch_bounds__(256, 4) crt_kernel(int64_t row0, int64_t rows,
   const uint32_t* W = reinterpret_cast<const uint32_t*>(Wb);
   const int ai = alpha[i];
   constexpr int NG = (MAXS + 3) / 4;  // channel groups of four
-  constexpr int NB = 4 * NL;          // byte limbs of Y
-  static_assert(NBC <= NB, "coefficient bytes within the limbs");
+  constexpr int NL16 = 2 * NL;        // 16-bit limbs of X
+  static_assert(NBC <= 2 * NL16, "coefficient bytes within the limbs");
   for (int64_t jg = jg0 + blockIdx.y; jg < jg1; jg += gridDim.y) {
     const int64_t base = jg * p_total + i;
     uint32_t wv[4 * NG];
@@ -227,40 +216,39 @@ __global__ void __launch_bounds__(256, 4) crt_kernel(int64_t row0, int64_t rows,
       // for t >= 1 (256 divides it), so only the first group takes b = 0
       // (no guards on s: the words past s and the table bytes past each M/m_t
       // are zero)
-      uint32_t S[NB];
+      uint32_t S[2 * NL16];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) S[b] = 0;
+      for (int b = 0; b < 2 * NL16; ++b) S[b] = 0;
 #pragma unroll
       for (int g = 0; g < NG; ++g)
 #pragma unroll
         for (int b = 0; b < NBC; ++b)
           if (b > 0 || g == 0) S[b] = __dp4a(wv[4 * g + v], cc.L4[g][b], S[b]);
-      // unnormalised 32-bit limbs of Y (each < 2^46)
-      uint64_t Y[NL];
+      // Y / M in float: each S_b < 2^20 converts exactly; the error is a few
+      // 2^-20, far below the 2^-12 margin used below.  k = RN_even(Y / M) by
+      // adding 1.5 2^23 (the float's integer part then sits in its low bits).
+      float yq = 0.0f;
 #pragma unroll
-      for (int q = 0; q < NL; ++q) {
-        const uint32_t lo = S[4 * q] + (S[4 * q + 1] << 8);
-        const uint32_t hi = S[4 * q + 2] + (S[4 * q + 3] << 8);
-        Y[q] = (static_cast<uint64_t>(hi) << 16) + lo;
-      }
-      // Y / M in float from every limb that can move it by 2^-49 or more:
-      // relative error a few 2^-24, far below the 2^-12 margin used below
-      float ye = 0.0f;
-#pragma unroll
-      for (int q = 0; q < NL; ++q)
-        if (q >= cc.est_lo) ye += __ull2float_rn(Y[q]) * __int_as_float((127 + 32 * (q - NL + 1)) << 23);
-      const float yq = ye * cc.inv_Ms;
-      const float kf = rintf(yq);
-      const int kq = static_cast<int>(kf);
+      for (int b = EB0; b < NBC; ++b) yq = __fmaf_rn(__uint2float_rn(S[b]), cc.est_f[b], yq);
+      const float tq = yq + 12582912.0f;
+      const int kq = __float_as_int(tq) - 0x4B400000;
+      const float kf = tq - 12582912.0f;
+      // X = Y - k M in 16-bit limbs: Z_q = S_2q + 2^8 S_2q+1 - k M16_q + carry
+      // (|Z_q| < 2^30), carry = floor(Z_q / 2^16); the last carry is the sign
+      // extension since |X| < M < 2^(32 NL - 1)
       uint32_t x[NL];
       {
-        int64_t carry = 0;
+        int32_t c = 0;
+        int32_t Z[NL16];
 #pragma unroll
-        for (int q = 0; q < NL; ++q) {
-          const int64_t z = static_cast<int64_t>(Y[q]) + carry - static_cast<int64_t>(kq) * cc.M[q];
-          x[q] = static_cast<uint32_t>(z);
-          carry = z >> 32;
+        for (int q = 0; q < NL16; ++q) {
+          const int32_t V = static_cast<int32_t>(S[2 * q] + (S[2 * q + 1] << 8));
+          Z[q] = V - kq * static_cast<int32_t>(cc.M16[q]) + c;
+          c = Z[q] >> 16;
         }
+#pragma unroll
+        for (int w = 0; w < NL; ++w)
+          x[w] = __byte_perm(static_cast<uint32_t>(Z[2 * w]), static_cast<uint32_t>(Z[2 * w + 1]), 0x5410u);
       }
       // exact correction into [-M/2, M/2), only near a half-integer Y / M
       if (fabsf(yq - kf) > 0.5f - 0x1p-12f) {
@@ -291,15 +279,15 @@ __global__ void __launch_bounds__(256, 4) crt_kernel(int64_t row0, int64_t rows,
           }
         }
       }
-      if (Xout) {
+      if constexpr (WX) {
         const bool neg = static_cast<int32_t>(x[NL - 1]) < 0;
         uint32_t ext[6];
 #pragma unroll
         for (int l = 0; l < 6; ++l) ext[l] = (l < NL) ? x[l] : (neg ? 0xFFFFFFFFu : 0u);
         uint64_t* xo = Xout + (j * p_total + i) * 3;
-        xo[0] = (static_cast<uint64_t>(ext[1]) << 32) | ext[0];
-        xo[1] = (static_cast<uint64_t>(ext[3]) << 32) | ext[2];
-        xo[2] = (static_cast<uint64_t>(ext[5]) << 32) | ext[4];
+        xo[0] = pack64(ext[1], ext[0]);
+        xo[1] = pack64(ext[3], ext[2]);
+        xo[2] = pack64(ext[5], ext[4]);
       }
       C[j * ldc + i] = round_x<NL>(x, ai + beta[j]);
     }
@@ -342,14 +330,27 @@ cudaError_t launch_crt(int64_t row0, int64_t rows, int64_t p_total, int64_t col0
   if (gy < 1) gy = 1;
   const dim3 b(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   const int nl = crt_limbs(s);
-  // exact instances for the common channel counts (fewer groups and byte
-  // limbs), else the limb-count buckets with MAXS - 1 coefficient bytes
-  if (s == 8) crt_kernel<8, 3, 7><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (s == 14) crt_kernel<14, 4, 13><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (s == 18) crt_kernel<18, 5, 17><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 3) crt_kernel<11, 3, 10><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else if (nl == 4) crt_kernel<15, 4, 14><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
-  else crt_kernel<20, 5, 19><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X);
+#define OZ2_CRT(MAXS, NL, NBC, EB0, MINB, WX) \
+  crt_kernel<MAXS, NL, NBC, EB0, MINB, WX><<<b, 256, 0, st>>>(row0, rows, p_total, jg0, jg1, r, cc, W, alpha, beta, C, ldc, X)
+  if (X) {
+    // checking path: one instance per word count
+    if (nl == 3) OZ2_CRT(11, 3, 10, 0, 4, true);
+    else if (nl == 4) OZ2_CRT(15, 4, 14, 5, 4, true);
+    else OZ2_CRT(20, 5, 19, 9, 3, true);
+  } else if (s == 8) {
+    OZ2_CRT(8, 3, 7, 1, 4, false);
+  } else if (s == 14) {
+    OZ2_CRT(14, 4, 13, 7, 4, false);
+  } else if (s == 18) {
+    OZ2_CRT(18, 5, 17, 11, 3, false);
+  } else if (nl == 3) {  // the other counts: buckets by word count, MAXS - 1 coefficient bytes
+    OZ2_CRT(11, 3, 10, 0, 4, false);
+  } else if (nl == 4) {
+    OZ2_CRT(15, 4, 14, 5, 4, false);
+  } else {
+    OZ2_CRT(20, 5, 19, 9, 3, false);
+  }
+#undef OZ2_CRT
   count_launches(1);
   return cudaGetLastError();
 }

@@ -49,8 +49,8 @@ struct CrtConsts {  // per-s CRT constants
   int m[kSMax];
   uint32_t M[kLimbs];             // M, 32-bit limbs
   uint32_t Mhalf[kLimbs];         // M/2 (M is even: 256 is always a modulus)
-  float inv_Ms;                   // 2^(32 (NL - 1)) / M, NL = crt_limbs(s)
-  int est_lo;                     // lowest 32-bit limb of Y the estimate of Y / M uses
+  uint32_t M16[kLimbs16];         // M, 16-bit limbs (one per word)
+  float est_f[2 * kLimbs16];      // 2^(8b) / M rounded to float: weight of byte-limb sum b in Y / M
   uint32_t L4[kSMax / 4][2 * kLimbs16];  // byte b of M/m_t for channels t = 4g .. 4g + 3, packed (dp4a); zero past s
 };
 
