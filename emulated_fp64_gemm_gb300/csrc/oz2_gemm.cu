@@ -185,37 +185,35 @@ __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, b
   if (!last) tmem_wait_st();
 }
 
-// CTA-pair bound GEMM, after the last chunk has been added into the running
-// sums (which then hold W itself, read here from sum_addr): the row maximum
-// of W 2^-v_j and the column maxima of W 2^-u_i over the warp's 32 rows, for
-// the 32-column blocks [cb0, cb1).  The keys are those of dyadic_key as a pair
-// of words, exponent word (floor(log2 value) + 4096, positive for every
-// nonzero entry) and normalised mantissa, compared lexicographically; a
-// column maximum is two 32-bit warp max reductions, first over the exponent
-// words, then over the mantissas of the lanes that hold that exponent.  The
-// tensor core is already working on the next unit's accumulator meanwhile.
-__device__ __forceinline__ void bound_final_keys2(uint32_t sum_addr, int64_t il, int64_t i, int64_t j0, int lane,
-                                                  const KParams& kp, int cb0, int cb1) {
+// CTA-pair bound GEMM, after the last chunk: from the running sums W_ij in
+// registers (this thread's row i, the NB 32-column blocks starting at block
+// cb0), the row maximum of W 2^-v_j and the column maxima of W 2^-u_i over
+// the warp's 32 rows.  The keys are those of dyadic_key as a pair of words,
+// exponent word (floor(log2 value) + 4096, positive for every nonzero entry)
+// and normalised mantissa, compared lexicographically; a column maximum is
+// two 32-bit warp max reductions, first over the exponent words, then over
+// the mantissas of the lanes that hold that exponent.  The tensor core is
+// already working on the next unit meanwhile.
+template <int NB>
+__device__ __forceinline__ void bound_final_keys_regs(const uint32_t (&w)[NB][32], int64_t il, int64_t i,
+                                                      int64_t j0, int lane, const KParams& kp, int cb0) {
   const bool row_ok = il < kp.p;
   const int ui = row_ok ? kp.u[i] : 0;
   uint32_t rhi = 0, rlo = 0;
-#pragma unroll 1
-  for (int cb = cb0; cb < cb1; ++cb) {
-    uint32_t w[32];
-    tmem_ld32(sum_addr + cb * 32, w);
-    const int64_t jl = j0 + cb * 32 + lane;  // this lane's column
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int64_t jl = j0 + (cb0 + b) * 32 + lane;  // this lane's column
     const int vl = (jl < kp.r) ? kp.v[jl] : 0;
-    tmem_wait_ld();
     uint32_t chi = 0, clo = 0;  // the maximum of column jl
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      const int64_t j = j0 + cb * 32 + k;
-      const uint32_t x = (row_ok && j < kp.r) ? w[k] : 0u;
+      const int64_t j = j0 + (cb0 + b) * 32 + k;
+      const uint32_t x = (row_ok && j < kp.r) ? w[b][k] : 0u;
       const int vj = __shfl_sync(0xffffffffu, vl, k);
-      const int b = 32 - __clz(static_cast<int>(x));  // bit length (0 for x = 0)
-      const uint32_t mant = x ? (x << (32 - b)) : 0u;
-      const uint32_t hr = x ? static_cast<uint32_t>(b - 1 - vj + 4096) : 0u;
-      const uint32_t hc = x ? static_cast<uint32_t>(b - 1 - ui + 4096) : 0u;
+      const int bl = 32 - __clz(static_cast<int>(x));  // bit length (0 for x = 0)
+      const uint32_t mant = x ? (x << (32 - bl)) : 0u;
+      const uint32_t hr = x ? static_cast<uint32_t>(bl - 1 - vj + 4096) : 0u;
+      const uint32_t hc = x ? static_cast<uint32_t>(bl - 1 - ui + 4096) : 0u;
       if (hr > rhi || (hr == rhi && mant > rlo)) {
         rhi = hr;
         rlo = mant;
@@ -816,6 +814,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
       int stage = 0;
       uint32_t phase = 0;
       uint32_t use[2] = {0, 0};
+      int bslot = 0;  // bound GEMM: the slot of the next chunk (chunks alternate)
       bool ok = true;
       for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
         const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
@@ -823,7 +822,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
         for (int c = 0; c < nch && ok; ++c) {
           const int kb0 = chunk_begin(c, nch, kp);
           const int kb1 = chunk_begin(c + 1, nch, kp);
-          for (int sl = 0; sl < U.ntile && ok; ++sl) {
+          for (int s0 = 0; s0 < U.ntile && ok; ++s0) {
+            const int sl = (KIND == kGemmBound) ? bslot : s0;
             if (!mbar_wait_cluster_bounded(smem_u32(&acce[sl]), (use[sl] & 1) ^ 1, abort_flag, kWaitLimitNs)) {
               ok = false;
               break;
@@ -853,6 +853,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
             }
             if (ok) mma_commit_pair(smem_u32(&accf[sl]));
           }
+          if (KIND == kGemmBound) bslot ^= 1;
         }
       }
       if (!ok) {
@@ -870,6 +871,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t use[2] = {0, 0};
+    int bslot = 0;  // bound GEMM: the slot of the next chunk
+    // bound GEMM: this thread's int32 running sums W_ij (its row, the
+    // NBLK 32-column blocks of its part of the tile)
+    constexpr int NBLK = (KIND == kGemmBound) ? BN / 32 / NPART : 1;
+    uint32_t bsum[NBLK][32];
     bool ok = true;
     for (int64_t u = cluster; u < kp.units && ok; u += nclusters) {
       const Unit2 U = decode_unit2<KIND == kGemmBound>(u, kp);
@@ -881,7 +887,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
       const int nch = unit_nchunks(U.t, kp);
       for (int c = 0; c < nch && ok; ++c) {
         const bool last = (c == nch - 1);
-        for (int sl = 0; sl < U.ntile; ++sl) {
+        for (int s0 = 0; s0 < U.ntile; ++s0) {
+          const int sl = (KIND == kGemmBound) ? bslot : s0;
           const bool got = mbar_wait_cluster_bounded(smem_u32(&accf[sl]), use[sl] & 1, abort_flag, kWaitLimitNs);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
@@ -890,17 +897,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * epi_warps2
           ++use[sl];
           tc_fence_after();
           const uint32_t acc_addr = tmem_base + lane_addr + static_cast<uint32_t>(sl * 256);
-          const int64_t j0 = kp.col0 + static_cast<int64_t>(U.tn0 + sl) * BN;
+          const int64_t j0 = kp.col0 + static_cast<int64_t>((KIND == kGemmBound ? U.tn0 : U.tn0 + sl)) * BN;
           if (KIND == kGemmBound) {
-            // every chunk, the last included: its sums into the int32 running
-            // sums; then the accumulator goes back to the MMA, and after the
-            // last chunk the keys are taken from the running sums (= W)
-            const int cb0 = part * (BN / 32 / NPART), cb1 = (part + 1) * (BN / 32 / NPART);
-            bound_epilogue_chunk<BN>(acc_addr, c, false, il, i, j0, lane, kp, cb0, cb1);
+            // every chunk, the last included: the chunk's sums (exact fp32
+            // integers) of this warp's columns into the int32 running sums in
+            // registers; the slot then goes back to the MMA, which is already
+            // working on the next chunk in the other slot.  After the last
+            // chunk the keys are taken from the running sums (= W).
+            const int cb0 = part * NBLK;
+#pragma unroll
+            for (int b = 0; b < NBLK; ++b) {
+              uint32_t v[32];
+              tmem_ld32(acc_addr + (cb0 + b) * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const uint32_t add = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[k])));
+                bsum[b][k] = (c == 0) ? add : bsum[b][k] + add;
+              }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&acce[sl]), 0));
-            if (last) bound_final_keys2(acc_addr + BN, il, i, j0, lane, kp, cb0, cb1);
+            if (KIND == kGemmBound) bslot ^= 1;
+            if (last) bound_final_keys_regs<NBLK>(bsum, il, i, j0, lane, kp, cb0);
             continue;
           } else if (!last) {
 #pragma unroll 1
