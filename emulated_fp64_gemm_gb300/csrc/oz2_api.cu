@@ -555,7 +555,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
         const int64_t c0 = cfirst[c];
         if (staged) OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_upB[c], 0));
         OZ2_CU(launch_cols_fused_fast(B + c0 * ldb, q, cfirst[c + 1] - c0, ldb, qp, r, hc->bound, hc->mod,
-                                      ds->pow2mod, max_bits, beta + c0, planesB + c0 * qp, wsp->aux));
+                                      ds->pow2mod, max_bits, beta + c0, planesB + c0 * qp, ds->err, wsp->aux));
         OZ2_CU(cudaEventRecord(wsp->ev_bpart[c], wsp->aux));
       }
     } else {
@@ -572,7 +572,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     OZ2_CU(cudaEventRecord(wsp->ev_start, st));
     OZ2_CU(cudaStreamWaitEvent(wsp->aux, wsp->ev_start, 0));
     OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, r, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
-                                  wsp->aux));
+                                  ds->err, wsp->aux));
     OZ2_CU(cudaEventRecord(wsp->ev_bready, wsp->aux));
     OZ2_CU(launch_rows_fused_fast(A, p, q, lda, qp, p, hc->bound, hc->mod, ds->pow2mod, max_bits, alpha, planesA,
                                   st));
@@ -590,7 +590,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     }
     if (fused_b) {
       OZ2_CU(launch_cols_fused_fast(B, q, r, ldb, qp, r, hc->bound, hc->mod, ds->pow2mod, max_bits, beta, planesB,
-                                    st));
+                                    ds->err, st));
       b_planes_done = true;
     } else {
       OZ2_CU(launch_fast_exponents_cols(sa, hc->bound, amaxB, reinterpret_cast<uint64_t*>(at(L.sumB)), beta,

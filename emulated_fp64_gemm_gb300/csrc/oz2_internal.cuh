@@ -128,7 +128,7 @@ bool cols_fused_fast_supported(int64_t q);
 cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
                                    int64_t plane_cols, const BoundConsts& bc, const ModConsts& mc,
                                    const uint8_t* pow2mod, int max_bits, int32_t* beta, uint16_t* planes,
-                                   cudaStream_t st);
+                                   int* err, cudaStream_t st);
 
 // fast mode, A side for short rows in one read of A: alpha and the residue
 // planes of `rows` rows (identical to launch_fast_exponents_rows followed by

@@ -244,44 +244,70 @@ __global__ void __launch_bounds__(256, ResOcc<NW>::kMinBlocks) residue_cols_kern
   }
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from global memory to this CTA's
+// shared memory, both addresses 16-byte aligned, counted on an mbarrier.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+constexpr uint64_t kStatsWaitNs = 2ull * 1000 * 1000 * 1000;  // 2 s: a 64 KB copy takes microseconds
+
 // Fast mode, statistics of B's columns in one read (2048 < q <= 8192): one
-// block per column; thread t holds the column's elements [2048 c + 8 t, +8)
-// for c < NCH in registers, so the maximum and then the sum of squares come
-// from one read of B.  Writes beta_j; the residue planes follow from
+// block per column.  The column (contiguous, column-major B) is brought into
+// shared memory by one bulk copy of its 16-byte aligned middle; the one
+// element before it (a column starting 8 bytes past a 16-byte boundary) and
+// the one after it are plain loads.  The maximum and then the sum of squares
+// are taken from shared memory, so three columns per SM are in flight while
+// others compute.  Writes beta_j; the residue planes follow from
 // residue_cols_kernel.  Results are identical to amax_cols + sumsq_cols +
-// fast_exp: the reductions are exact integer maxima and sums.
-template <int NCH>
-__global__ void __launch_bounds__(256, 2) stats_cols_fast_kernel(const double* __restrict__ B, int64_t q, int64_t ldb,
-                                                              BoundConsts bc, int32_t* __restrict__ beta) {
+// fast_exp: the reductions are exact integer maxima and sums.  A copy that
+// has not landed within kStatsWaitNs sets the timeout bit in *err, and the
+// block waits (bounded again) for it before leaving.
+__global__ void __launch_bounds__(256, 3) stats_cols_bulk_kernel(const double* __restrict__ B, int64_t q,
+                                                                 int64_t ldb, BoundConsts bc,
+                                                                 int32_t* __restrict__ beta, int* err) {
+  extern __shared__ __align__(16) uint8_t col_smem[];
   __shared__ uint64_t red[8];
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t j = blockIdx.x;
   const double* col = B + j * ldb;
-  const bool vec = (reinterpret_cast<uintptr_t>(col) & 15) == 0;
-  double x[NCH][8];
-#pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    const int64_t l0 = c * 2048ll + tid * 8ll;
-    if (vec && l0 + 8 <= q) {
-#pragma unroll
-      for (int k = 0; k < 8; k += 2) {
-        const double2 v = __ldg(reinterpret_cast<const double2*>(col + l0 + k));
-        x[c][k] = v.x;
-        x[c][k + 1] = v.y;
-      }
+  const int h = static_cast<int>((reinterpret_cast<uintptr_t>(col) >> 3) & 1);  // elements before the aligned middle
+  const int64_t nmid = ((q - h) / 2) * 2;                                         // elements in it (even)
+  const double* buf = reinterpret_cast<const double*>(col_smem);                // column element h + l at buf[l]
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (nmid > 0) {
+      mbar_arrive_expect_tx(smem_u32(&bar), static_cast<uint32_t>(nmid * 8));
+      bulk_copy_g2s(smem_u32(col_smem), col + h, static_cast<uint32_t>(nmid * 8), smem_u32(&bar));
     } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) x[c][k] = (l0 + k < q) ? __ldg(col + l0 + k) : 0.0;
+      mbar_arrive(smem_u32(&bar));
     }
   }
-  uint64_t m = 0;
-#pragma unroll
-  for (int c = 0; c < NCH; ++c)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x[c][k])) & ~(1ull << 63);
-      m = b > m ? b : m;
+  double xe = 0.0;  // the element outside the aligned middle, if any, for threads 0 (head) and 1 (tail)
+  if (tid == 0 && h) xe = __ldg(col);
+  if (tid == 1 && h + nmid < q) xe = __ldg(col + q - 1);
+  const bool got = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, kStatsWaitNs);
+  if (__syncthreads_or(!got)) {
+    if (tid == 0) {
+      atomicOr(err, kErrTimeout);
+      mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, kStatsWaitNs);  // the copy still in flight
     }
+    return;
+  }
+  uint64_t m = static_cast<uint64_t>(__double_as_longlong(xe)) & ~(1ull << 63);
+  for (int64_t l = tid; l < nmid; l += 256) {
+    const uint64_t b = static_cast<uint64_t>(__double_as_longlong(buf[l])) & ~(1ull << 63);
+    m = b > m ? b : m;
+  }
   for (int o = 16; o; o >>= 1) {
     const uint64_t y = __shfl_xor_sync(0xffffffffu, m, o);
     m = y > m ? y : m;
@@ -292,14 +318,12 @@ __global__ void __launch_bounds__(256, 2) stats_cols_fast_kernel(const double* _
   for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
   __syncthreads();
   const int e = exp_of_bits(m);
-  uint64_t sum = 0;
-#pragma unroll
-  for (int c = 0; c < NCH; ++c)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t cs = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(x[c][k])), kF - e);
-      sum += static_cast<uint64_t>(cs) * cs;
-    }
+  const uint32_t ce = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(xe)), kF - e);
+  uint64_t sum = static_cast<uint64_t>(ce) * ce;
+  for (int64_t l = tid; l < nmid; l += 256) {
+    const uint32_t cs = ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(buf[l])), kF - e);
+    sum += static_cast<uint64_t>(cs) * cs;
+  }
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane == 0) red[warp] = sum;
   __syncthreads();
@@ -543,7 +567,7 @@ bool cols_fused_fast_supported(int64_t q) { return q <= 8192; }
 cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, int64_t ldb, int64_t qp,
                                    int64_t plane_cols, const BoundConsts& bc, const ModConsts& mc,
                                    const uint8_t* pow2mod, int max_bits, int32_t* beta, uint16_t* planes,
-                                   cudaStream_t st) {
+                                   int* err, cudaStream_t st) {
   if (!cols_fused_fast_supported(q) || ncols < 1 || ncols > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(ncols));
   if (qp <= 2048) {
@@ -558,8 +582,11 @@ cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, in
   // longer columns: the statistics from one read of B, then the residue kernel
   // (a second read of B; faster than one kernel that holds the column through
   // the residues, whose register footprint leaves two blocks per SM)
-  if (qp <= 4096) stats_cols_fast_kernel<2><<<g, 256, 0, st>>>(B, q, ldb, bc, beta);
-  else stats_cols_fast_kernel<4><<<g, 256, 0, st>>>(B, q, ldb, bc, beta);
+  const int smem = static_cast<int>(q * 8);  // <= 64 KB: the aligned middle of one column
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(stats_cols_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8192 * 8);
+  if (attr != cudaSuccess) return attr;
+  stats_cols_bulk_kernel<<<g, 256, smem, st>>>(B, q, ldb, bc, beta, err);
   count_launches(1);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
