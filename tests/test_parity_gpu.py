@@ -246,6 +246,35 @@ def test_host_entry_point_four_column_parts(oz2):
     assert ulp_distance(Ch[ii, jj], ref["C"]) <= ULP_TOL
 
 
+@pytest.mark.parametrize("p,q,r", [(5000, 700, 6100), (2049, 3000, 9000), (4100, 2100, 2048)])
+def test_host_entry_point_large_strided(oz2, p, q, r):
+    """Fast mode with p, r >= 2048 and ragged sizes: the host entry point's
+    staged uploads, overlapped row blocks and split first and last blocks
+    (A's one-read kernel for q <= 2048, its three kernels above; B's bulk-copy
+    statistics).  Strided host A, B and C (lda > p, ldb > q, ldc > p); C must
+    equal the device entry point's bit for bit, and sampled entries the
+    oracle's, and nothing outside C may be written."""
+    A, B = make_matrices(p, q, r, 0.5, 90 + q % 7)
+    hAbig = torch.zeros((q, p + 8), dtype=torch.float64)
+    hAbig.t()[:p] = torch.from_numpy(A)
+    hBbig = torch.zeros((r, q + 4), dtype=torch.float64)
+    hBbig.t()[:q] = torch.from_numpy(B)
+    hA = hAbig.pin_memory().t()[:p]
+    hB = hBbig.pin_memory().t()[:q]
+    big = torch.full((r, p + 16), 7.0, dtype=torch.float64).pin_memory()
+    hC = big.t()[:p]
+    oz2.dgemm_host(hA, hB, 14, "fast", out=hC)
+    Cd = oz2.dgemm(_dev(A), _dev(B), 14, "fast").cpu().numpy()
+    np.testing.assert_array_equal(hC.numpy(), Cd)
+    assert np.all(big.t()[p:].numpy() == 7.0)
+    rng = np.random.default_rng(p + r)
+    ii = np.concatenate([rng.integers(0, p, 60), [0, 1023, 1024, p - 1]])
+    jj = np.concatenate([rng.integers(0, r, 60), [0, 1023, 1024, r - 1]])
+    ref = oracle.oracle_entries(A, B, 14, "fast", ii, jj)
+    assert ulp_distance(hC.numpy()[ii, jj], ref["C"]) <= ULP_TOL
+    assert oz2.last_error() == 0
+
+
 @pytest.mark.parametrize("mode", ["fast", "accu"])
 def test_single_cta_gemm_selection_matches(oz2, mode, monkeypatch):
     """OZ2_GEMM_1SM=1 selects the single-CTA tcgen05 kernel for the modular and
