@@ -583,7 +583,8 @@ cudaError_t launch_cols_fused_fast(const double* B, int64_t q, int64_t ncols, in
   // (a second read of B; faster than one kernel that holds the column through
   // the residues, whose register footprint leaves two blocks per SM)
   const int smem = static_cast<int>(q * 8);  // <= 64 KB: the aligned middle of one column
-  static const cudaError_t attr =
+  // (set on every launch: the attribute belongs to the current device)
+  const cudaError_t attr =
       cudaFuncSetAttribute(stats_cols_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8192 * 8);
   if (attr != cudaSuccess) return attr;
   stats_cols_bulk_kernel<<<g, 256, smem, st>>>(B, q, ldb, bc, beta, err);
