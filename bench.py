@@ -81,6 +81,10 @@ def parse_args(argv=None):
     ap.add_argument("--mode", choices=["fast", "accu"], default=None, help="bound mode (overrides the workload's)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every s in %s at n in %s, fast and accu (one JSON line each)" % (SWEEP_S, SWEEP_N))
+    ap.add_argument("--sweep-n", type=str, default=None,
+                    help="comma-separated n for --sweep (default %s)" % ",".join(map(str, SWEEP_N)))
+    ap.add_argument("--sweep-s", type=str, default=None,
+                    help="comma-separated s for --sweep (default %s)" % ",".join(map(str, SWEEP_S)))
     ap.add_argument("--stages-once", action="store_true",
                     help="one call of the stage-timed entry point (each stage alone), e.g. under a profiler")
     ap.add_argument("--no-e2e", action="store_true")
@@ -617,10 +621,23 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def sweep_sets(args):
+    """(n values, s values) of --sweep: --sweep-n / --sweep-s, else SWEEP_N / SWEEP_S."""
+    ns = tuple(int(x) for x in args.sweep_n.split(",")) if args.sweep_n else SWEEP_N
+    ss = tuple(int(x) for x in args.sweep_s.split(",")) if args.sweep_s else SWEEP_S
+    for s in ss:
+        if not 2 <= s <= 20:
+            raise SystemExit(f"--sweep-s: s = {s} outside 2..20")
+    for n in ns:
+        if n < 1:
+            raise SystemExit(f"--sweep-n: n = {n} must be positive")
+    return ns, ss
+
+
 def run_sweep(args):
     """ms per call (clean pass) and per stage (stage-timed pass) for every s in
-    SWEEP_S at n in SWEEP_N, fast and accu, phi = 0.5, seed 123456: one JSON
-    line per configuration."""
+    SWEEP_S at n in SWEEP_N (or --sweep-s / --sweep-n), fast and accu,
+    phi = 0.5, seed 123456: one JSON line per configuration."""
     import torch
 
     import __graft_entry__ as entry
@@ -630,14 +647,15 @@ def run_sweep(args):
     import emulated_fp64_gemm_gb300 as oz2
 
     stream = torch.cuda.current_stream()
-    for n in SWEEP_N:
+    sweep_n, sweep_s = sweep_sets(args)
+    for n in sweep_n:
         A, B = make_matrices(n, n, n, 0.5, 123456)
         dA = torch.from_numpy(A).cuda()
         dB = torch.from_numpy(B).cuda()
         C = torch.empty((n, n), dtype=torch.float64, device="cuda").t()
         steps = max(3, min(args.steps, 30))
         for mode in ("fast", "accu"):
-            for s in SWEEP_S:
+            for s in sweep_s:
                 w = Workload(f"n{n}_s{s}_{mode}", n, n, n, s, mode, 0.5, 123456)
                 for _ in range(3):
                     oz2.dgemm(dA, dB, s, mode, out=C)

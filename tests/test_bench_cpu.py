@@ -125,3 +125,12 @@ def test_s_and_mode_overrides_rename_the_workload():
     assert line["vs_baseline"] is None
     same = bench.resolve_workload(bench.parse_args([]))
     assert same is bench.WORKLOADS["n8192_s14_fast"]
+
+
+def test_sweep_sets_default_and_override():
+    args = bench.parse_args(["--sweep"])
+    assert bench.sweep_sets(args) == (bench.SWEEP_N, bench.SWEEP_S)
+    args = bench.parse_args(["--sweep", "--sweep-n", "2048,16384", "--sweep-s", "14,15,18"])
+    assert bench.sweep_sets(args) == ((2048, 16384), (14, 15, 18))
+    with pytest.raises(SystemExit):
+        bench.sweep_sets(bench.parse_args(["--sweep", "--sweep-s", "21"]))
