@@ -103,15 +103,7 @@ __device__ __forceinline__ constexpr uint32_t instr_desc() {
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-// Order-preserving key of the dyadic value w * 2^-x (w >= 0, w < 2^31).
-__device__ __forceinline__ uint64_t dyadic_key(uint32_t w, int x) {
-  if (w == 0) return 0;
-  const int b = 32 - __clz(static_cast<int>(w));  // bit length
-  const int E = b - 1 - x;                         // floor(log2 value)
-  return (static_cast<uint64_t>(E + 4096) << 32) | static_cast<uint64_t>(w << (32 - b));
-}
-
-// Column maxima over a warp's 32 rows: each lane holds 32 keys (one per
+// Column maxima over a warp's 32 rows: each lane holds 32 values (one per
 // column).  Five exchange steps halve the columns a lane keeps (16, 8, 4, 2,
 // 1 keys cross per step): at the step with offset o a lane keeps the upper
 // half of its remaining columns when its own bit o is set and sends the other
@@ -135,17 +127,15 @@ __device__ __forceinline__ uint64_t warp_column_max(uint64_t (&kc)[32], int lane
 // Epilogue of the accu bound GEMM for one BNc-column tile slot of one thread's
 // row: the chunk's fp32 sums (exact integers below 2^24) are added into the
 // int32 running sums held BNc columns further on in tensor memory.  After the
-// last chunk each entry W_ij of the row becomes the order-preserving keys of
-// W 2^-v_j (row maximum) and W 2^-u_i (column maximum over the warp's 32 rows),
-// and the maxima are taken with 64-bit atomics.  The thread handles the
-// 32-column blocks [cb0, cb1) of the slot.
+// last chunk the running sums are the bound products Wbar_ij, whose row
+// maximum and column maxima (over the warp's 32 rows) go to rowkey / colkey
+// by atomics.  The thread handles the 32-column blocks [cb0, cb1) of the slot.
 template <int BNc>
 __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, bool last, int64_t il, int64_t i,
                                                      int64_t j0, int lane, const KParams& kp, int cb0 = 0,
                                                      int cb1 = BNc / 32) {
   const uint32_t sum_addr = acc_addr + BNc;
   const bool row_ok = il < kp.p;
-  const int ui = (last && row_ok) ? kp.u[i] : 0;
   uint64_t rmax = 0;
 #pragma unroll 1
   for (int cb = cb0; cb < cb1; ++cb) {
@@ -161,18 +151,14 @@ __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, b
     if (!last) {
       tmem_st32(sum_addr + cb * 32, sacc);
     } else {
-      // row: max_j key(W_ij 2^-v_j); column: max_i key(W_ij 2^-u_i)
+      // row: max_j Wbar_ij; column: max_i Wbar_ij
       uint64_t kc[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const int64_t j = j0 + cb * 32 + k;
-        const bool valid = row_ok && (j < kp.r);
-        const uint32_t w = valid ? sacc[k] : 0u;
-        if (valid) {
-          const uint64_t kr = dyadic_key(w, kp.v[j]);
-          rmax = kr > rmax ? kr : rmax;
-        }
-        kc[k] = valid ? dyadic_key(w, ui) : 0ull;
+        const uint64_t w = (row_ok && j < kp.r) ? sacc[k] : 0u;
+        rmax = w > rmax ? w : rmax;
+        kc[k] = w;
       }
       const uint64_t cmax = warp_column_max(kc, lane);
       const int64_t jl = j0 + cb * 32 + lane;
@@ -185,52 +171,34 @@ __device__ __forceinline__ void bound_epilogue_chunk(uint32_t acc_addr, int c, b
   if (!last) tmem_wait_st();
 }
 
-// CTA-pair bound GEMM, after the last chunk: from the running sums W_ij in
-// registers (this thread's row i, the NB 32-column blocks starting at block
-// cb0), the row maximum of W 2^-v_j and the column maxima of W 2^-u_i over
-// the warp's 32 rows.  The keys are those of dyadic_key as a pair of words,
-// exponent word (floor(log2 value) + 4096, positive for every nonzero entry)
-// and normalised mantissa, compared lexicographically; a column maximum is
-// two 32-bit warp max reductions, first over the exponent words, then over
-// the mantissas of the lanes that hold that exponent.  The tensor core is
-// already working on the next unit meanwhile.
+// CTA-pair bound GEMM, after the last chunk: from the running sums Wbar_ij
+// in registers (this thread's row i, the NB 32-column blocks starting at
+// block cb0), the row maximum and the column maxima over the warp's 32 rows
+// (one 32-bit warp max reduction per column), each taken into rowkey /
+// colkey with one atomic.  The tensor core is already working on the next
+// unit meanwhile.
 template <int NB>
 __device__ __forceinline__ void bound_final_keys_regs(const uint32_t (&w)[NB][32], int64_t il, int64_t i,
                                                       int64_t j0, int lane, const KParams& kp, int cb0) {
   const bool row_ok = il < kp.p;
-  const int ui = row_ok ? kp.u[i] : 0;
-  uint32_t rhi = 0, rlo = 0;
+  uint32_t rmax = 0;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const int64_t jl = j0 + (cb0 + b) * 32 + lane;  // this lane's column
-    const int vl = (jl < kp.r) ? kp.v[jl] : 0;
-    uint32_t chi = 0, clo = 0;  // the maximum of column jl
+    uint32_t cmax = 0;                              // the maximum of column jl
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       const int64_t j = j0 + (cb0 + b) * 32 + k;
       const uint32_t x = (row_ok && j < kp.r) ? w[b][k] : 0u;
-      const int vj = __shfl_sync(0xffffffffu, vl, k);
-      const int bl = 32 - __clz(static_cast<int>(x));  // bit length (0 for x = 0)
-      const uint32_t mant = x ? (x << (32 - bl)) : 0u;
-      const uint32_t hr = x ? static_cast<uint32_t>(bl - 1 - vj + 4096) : 0u;
-      const uint32_t hc = x ? static_cast<uint32_t>(bl - 1 - ui + 4096) : 0u;
-      if (hr > rhi || (hr == rhi && mant > rlo)) {
-        rhi = hr;
-        rlo = mant;
-      }
-      const uint32_t mh = __reduce_max_sync(0xffffffffu, hc);
-      const uint32_t ml = __reduce_max_sync(0xffffffffu, hc == mh ? mant : 0u);
-      if (lane == k) {
-        chi = mh;
-        clo = ml;
-      }
+      rmax = x > rmax ? x : rmax;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, x);
+      if (lane == k) cmax = m;
     }
-    if ((chi | clo) != 0 && jl < kp.r)
-      atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + jl),
-                (static_cast<unsigned long long>(chi) << 32) | clo);
+    if (cmax != 0 && jl < kp.r)
+      atomicMax(reinterpret_cast<unsigned long long*>(kp.colkey + jl), static_cast<unsigned long long>(cmax));
   }
-  if ((rhi | rlo) != 0)
-    atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), (static_cast<unsigned long long>(rhi) << 32) | rlo);
+  if (rmax != 0)
+    atomicMax(reinterpret_cast<unsigned long long*>(kp.rowkey + i), static_cast<unsigned long long>(rmax));
 }
 
 // K-chunks of a unit of channel t.
@@ -701,8 +669,9 @@ __device__ __forceinline__ Unit2 decode_unit2(int64_t u, const KParams& kp) {
 
 // Epilogue warps of the CTA-pair kernel: four for the modular GEMMs (one per
 // TMEM lane quadrant); eight for the bound GEMM, two per quadrant, each taking
-// half of a slot's columns, because its final epilogue (dyadic keys, column
-// maxima by shuffles, atomics) is latency-bound with one warp per scheduler.
+// half of a slot's columns: each holds its columns' int32 running sums in
+// registers (128 per thread), and its final step (column maxima by warp
+// reductions, atomics) is latency-bound with one warp per scheduler.
 template <int KIND>
 __host__ __device__ constexpr int epi_warps2() {
   return KIND == kGemmBound ? 8 : 4;

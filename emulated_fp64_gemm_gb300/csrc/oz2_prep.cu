@@ -308,25 +308,24 @@ __global__ void __launch_bounds__(256, 2) fused_cols_bound_kernel(const double* 
   }
 }
 
-// accu exponents from the max keys of the bound GEMM.  A key encodes the
-// dyadic value w 2^-x (w < 2^31) as ((floor(log2) + 4096) << 32) | mantissa
-// normalised to 32 bits; 0 encodes zero.  The row value is
-// max_j Wbar_ij 2^-v_j, so U_i = value 2^-u_i; likewise for columns.
+// accu exponents ("Profiling Ozaki II" §2 and §5.1: the row and column
+// maxima of the bound output give the final scale exponents), with the
+// maxima taken in the quantised scale: for row i, R_i = max_j Wbar_ij (from
+// the bound GEMM) and alpha_i = u_i + max {a : 4^a R_i <= L}; for column j,
+// beta_j = v_j + max {b : 4^b K_j <= L} with K_j = max_i Wbar_ij; 0 for a
+// zero row or column.  Then 2^(alpha_i + beta_j) (|A||B|)_ij <=
+// 2^(a_i + b_j) Wbar_ij <= sqrt(4^a_i R_i 4^b_j K_j) <= L.
 __global__ void accu_exp_kernel(const uint64_t* __restrict__ key, const int32_t* __restrict__ qexp,
                                 int64_t n, BoundConsts bc, int32_t* __restrict__ out) {
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (i >= n) return;
-  const uint64_t k = key[i];
+  const uint64_t k = key[i];  // the row (column) maximum of Wbar
   if (k == 0) {
     out[i] = 0;
     return;
   }
-  const int E = static_cast<int>(k >> 32) - 4096;        // value = mant32 * 2^(E - 31)
-  const uint64_t mant = k & 0xffffffffull;
-  const int h = max_shift_le_L(mant, bc);                // mant 2^h <= L
-  // 4^a mant 2^(E - 31 - u) <= L  <=>  2a + E - 31 - u <= h
-  const int num = h - E + 31 + qexp[i];
-  out[i] = num >> 1;                                     // floor
+  // 4^a k <= L  <=>  k 2^(2a) <= L  <=>  2a <= h
+  out[i] = qexp[i] + (max_shift_le_L(k, bc) >> 1);  // u + floor(h / 2)
 }
 
 __global__ void planes_to_int8_kernel(const uint16_t* __restrict__ planes, int64_t rows, int64_t q,

@@ -19,8 +19,9 @@
  *   O2  exponents.  fast: e = floor(log2 max|x|) + 1,
  *       S = sum ceil(|x| 2^(20 - e))^2 (exact), alpha = max {a : 4^a S 4^(e-20) <= L}.
  *       accu: u = max {u : ceil(max|x| 2^u) <= 127}, Abar = ceil(|A| 2^u),
- *       Bbar likewise with v, Wbar = Abar Bbar (exact), U_i = max_j Wbar_ij 2^-(u_i+v_j),
- *       V_j = max_i (same), alpha_i = max {a : 4^a U_i <= L}, beta_j likewise.
+ *       Bbar likewise with v, Wbar = Abar Bbar (exact); R_i = max_j Wbar_ij,
+ *       K_j = max_i Wbar_ij (maxima of the bound in the quantised scale),
+ *       alpha_i = u_i + max {a : 4^a R_i <= L}, beta_j = v_j + max {b : 4^b K_j <= L}.
  *   O3  A' = trunc(2^alpha A), B' = trunc(B 2^beta), toward zero.
  *   O4  rho_m(x) = ((x + floor(m/2)) mod m) - floor(m/2) for every modulus.
  *   O5  P_t = A_t B_t exactly (64-bit sums).
@@ -454,61 +455,30 @@ static void bound_quant_task(void* ctx, int64_t task) {
   else x->v[k] = u;
 }
 
-/* W 2^-e1 vs W' 2^-e2 (W, W' >= 0): -1, 0, 1 */
-static int cmp_dyadic(int64_t w1, int e1, int64_t w2, int e2) {
-  if (w1 == 0 || w2 == 0) return (w1 > 0) - (w2 > 0);
-  big a, b;
-  big_from_u128(&a, (unsigned __int128)w1);
-  big_from_u128(&b, (unsigned __int128)w2);
-  /* compare w1 2^(e2 - e1) with w2 via leading-bit positions, then exactly */
-  long la = (long)big_bitlen(&a) - e1, lb = (long)big_bitlen(&b) - e2;
-  if (la != lb) return la < lb ? -1 : 1;
-  /* w1 2^-e1 vs w2 2^-e2  <=>  w1 2^(e2 - e1) vs w2 (|e2 - e1| < 32 here) */
-  if (e2 > e1) big_shl(&a, e2 - e1);
-  else big_shl(&b, e1 - e2);
-  return big_cmp(&a, &b);
-}
-
-static int32_t accu_exponent_of(const consts* c, int64_t w, int e) {
-  /* 4^a w 2^-e <= L  <=>  w 2^(2a - e) <= L  <=>  2a <= h + e */
+/* max {a : 4^a w <= L} for an integer w > 0 (0 for w == 0) */
+static int32_t pow4_exponent_of(const consts* c, int64_t w) {
+  /* 4^a w <= L  <=>  w 2^(2a) <= L  <=>  2a <= h */
   if (w == 0) return 0;
   big Wb;
   big_from_u128(&Wb, (unsigned __int128)w);
-  return floor_div2(max_shift_le(&Wb, &c->L) + e);
+  return floor_div2(max_shift_le(&Wb, &c->L));
 }
 
+/* alpha_i = u_i + max {a : 4^a R_i <= L} with R_i = max_j Wbar_ij, the row
+ * maximum of the bound product in the quantised scale; beta_j likewise with
+ * v_j and K_j = max_i Wbar_ij.  0 for a zero row or column of Wbar. */
 static void accu_exp_task(void* ctx, int64_t task) {
   expctx* x = (expctx*)ctx;
-  if (task < x->p) { /* row i: max_j Wbar_ij 2^-(u_i + v_j) */
-    int64_t i = task;
-    int64_t bw = 0;
-    int be = 0;
-    for (int64_t j = 0; j < x->r; ++j) {
-      int64_t w = x->W[j * x->p + i];
-      int e = x->u[i] + x->v[j];
-      if (bw == 0 || cmp_dyadic(w, e, bw, be) > 0) {
-        if (w) {
-          bw = w;
-          be = e;
-        }
-      }
-    }
-    x->alpha[i] = accu_exponent_of(x->c, bw, be);
+  if (task < x->p) {
+    int64_t i = task, R = 0;
+    for (int64_t j = 0; j < x->r; ++j)
+      if (x->W[j * x->p + i] > R) R = x->W[j * x->p + i];
+    x->alpha[i] = R ? x->u[i] + pow4_exponent_of(x->c, R) : 0;
   } else {
-    int64_t j = task - x->p;
-    int64_t bw = 0;
-    int be = 0;
-    for (int64_t i = 0; i < x->p; ++i) {
-      int64_t w = x->W[j * x->p + i];
-      int e = x->u[i] + x->v[j];
-      if (bw == 0 || cmp_dyadic(w, e, bw, be) > 0) {
-        if (w) {
-          bw = w;
-          be = e;
-        }
-      }
-    }
-    x->beta[j] = accu_exponent_of(x->c, bw, be);
+    int64_t j = task - x->p, K = 0;
+    for (int64_t i = 0; i < x->p; ++i)
+      if (x->W[j * x->p + i] > K) K = x->W[j * x->p + i];
+    x->beta[j] = K ? x->v[j] + pow4_exponent_of(x->c, K) : 0;
   }
 }
 

@@ -229,62 +229,35 @@ def _exact_int_matmul(Ai: np.ndarray, Bi: np.ndarray) -> np.ndarray:
     return P.astype(np.int64)
 
 
-def _max_scaled(W: np.ndarray, w_exp: np.ndarray, axis: int):
-    """For each vector along axis: the index of the max of W * 2**(-w_exp).
-
-    w_exp broadcasts along axis (one exponent per entry of the reduced axis).
-    Exact: uses float64 ldexp where every value is a normal double that
-    round-trips, else exact Fractions.
-    """
-    W = np.asarray(W, dtype=np.int64)
-    vals = np.ldexp(W.astype(np.float64), -w_exp)
-    back = np.ldexp(vals, w_exp)
-    exact = np.all(np.isfinite(vals)) and np.all(back == W.astype(np.float64)) and np.all(
-        (vals == 0) | (np.abs(vals) >= np.finfo(np.float64).tiny))
-    if exact:
-        return np.argmax(vals, axis=axis)
-    # slow exact path
-    n_vec = W.shape[1 - axis]
-    idx = np.zeros(n_vec, dtype=np.int64)
-    we = np.broadcast_to(w_exp, W.shape)
-    for k in range(n_vec):
-        col = W[:, k] if axis == 0 else W[k, :]
-        ex = we[:, k] if axis == 0 else we[k, :]
-        best = None
-        for l in range(col.shape[0]):
-            v = Fraction(int(col[l])) * Fraction(2) ** (-int(ex[l]))
-            if best is None or v > best:
-                best, idx[k] = v, l
-    return idx
-
-
 def accu_exponents(A: np.ndarray, B: np.ndarray, L: int):
     """accu bound, [P] §2 and §5.1: one extra integer GEMM on |A|, |B|.
 
     Abar = ceil(|A| * 2**u_i) (rows), Bbar = ceil(|B| * 2**v_j) (columns),
-    Wbar = Abar Bbar (exact), W_ij = Wbar_ij * 2**(-u_i - v_j) >= (|A||B|)_ij.
+    Wbar = Abar Bbar (exact), so (|A||B|)_ij * 2**(u_i + v_j) <= Wbar_ij.
     Reading of "row/column maxima of the bound output -> final scale
-    exponents" as a geometric-mean split: U_i = max_j W_ij, V_j = max_i W_ij,
-      alpha_i = max { a : 4**a U_i <= L },  beta_j = max { b : 4**b V_j <= L }.
-    Then 2**(alpha_i + beta_j) W_ij <= sqrt(4**alpha_i U_i * 4**beta_j V_j) <= L.
+    exponents": the maxima are taken in the quantised scale,
+      R_i = max_j Wbar_ij,  K_j = max_i Wbar_ij,
+      alpha_i = u_i + max { a : 4**a R_i <= L },  beta_j = v_j + max { b : 4**b K_j <= L }
+    (0 for a zero row or column of Wbar).  Then
+      2**(alpha_i + beta_j) (|A||B|)_ij <= 2**(a_i + b_j) Wbar_ij
+                                        <= sqrt(4**a_i R_i * 4**b_j K_j) <= L,
+    and each row and column keeps its own scale u_i, v_j.
     Returns (alpha, beta, Abar, Bbar, u, v, Wbar).
     """
     Abar, u = bound_inputs(A, axis=1)
     Bbar, v = bound_inputs(B, axis=0)
     Wbar = _exact_int_matmul(Abar, Bbar)
     p, r = Wbar.shape
-    jmax = _max_scaled(Wbar, v[None, :], axis=1)  # per row: max_j Wbar_ij 2**-v_j
-    imax = _max_scaled(Wbar, u[:, None], axis=0)  # per column: max_i Wbar_ij 2**-u_i
+    R = Wbar.max(axis=1) if r else np.zeros(p, dtype=np.int64)
+    K = Wbar.max(axis=0) if p else np.zeros(r, dtype=np.int64)
     alpha = np.zeros(p, dtype=np.int64)
     beta = np.zeros(r, dtype=np.int64)
     for i in range(p):
-        j = int(jmax[i])
-        U = Fraction(int(Wbar[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) if r else Fraction(0)
-        alpha[i] = max_pow4_exponent(U, L)
+        if R[i] > 0:
+            alpha[i] = int(u[i]) + max_pow4_exponent(Fraction(int(R[i])), L)
     for j in range(r):
-        i = int(imax[j])
-        V = Fraction(int(Wbar[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) if p else Fraction(0)
-        beta[j] = max_pow4_exponent(V, L)
+        if K[j] > 0:
+            beta[j] = int(v[j]) + max_pow4_exponent(Fraction(int(K[j])), L)
     return alpha, beta, Abar, Bbar, u, v, Wbar
 
 

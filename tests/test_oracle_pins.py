@@ -250,11 +250,10 @@ def test_eq18_on_unit_matrices(mode):
 
 
 def test_exponents_scale_equivariant():
-    """fast: scaling row i of A by 2**c lowers alpha_i by c and leaves the rest.
-
-    accu (geometric-mean reading): scaling all of A by 4**c lowers every alpha
-    and every beta by c, so alpha_i + beta_j absorbs the whole factor.
-    """
+    """Both modes: scaling row i of A by 2**c lowers alpha_i by c and scaling
+    column j of B by 2**c lowers beta_j by c, leaving every other exponent
+    alone (accu: u_i shifts by c while Abar and Wbar stay the same, so each
+    row and column keeps its own scale)."""
     A, B = make_matrices(6, 9, 5, 1.0, 11)
     al, be, _ = oz.exponents(A, B, 14, "fast")
     A2 = A.copy()
@@ -271,10 +270,14 @@ def test_exponents_scale_equivariant():
     np.testing.assert_array_equal(al2, want_a)
     np.testing.assert_array_equal(be2, want_b)
     al, be, _ = oz.exponents(A, B, 14, "accu")
-    for c in (3, -5):
-        al2, be2, _ = oz.exponents(A * 4.0**c, B, 14, "accu")
-        np.testing.assert_array_equal(al2, al - c)
-        np.testing.assert_array_equal(be2, be - c)
+    al2, be2, _ = oz.exponents(A2, B2, 14, "accu")
+    want_a = al.copy()
+    want_a[2] -= 7
+    want_a[4] += 33
+    want_b = be.copy()
+    want_b[1] -= 12
+    np.testing.assert_array_equal(al2, want_a)
+    np.testing.assert_array_equal(be2, want_b)
 
 
 def test_fast_statistic_sandwich_and_near_maximality():
@@ -327,55 +330,11 @@ def test_fast_statistic_past_two_to_the_63(q):
     assert int(oz.fast_exponents(col, axis=0, L=L)[0]) == _max_pow4_brute(Fraction(q), L)
 
 
-def _max_scaled_brute(W, w_exp, axis):
-    """max along axis of Fraction(W) 2**-w_exp, by brute force over exact values."""
-    W = np.asarray(W)
-    we = np.broadcast_to(w_exp, W.shape)
-    n = W.shape[1 - axis]
-    out = []
-    for k in range(n):
-        vals = [Fraction(int(W[l, k] if axis == 0 else W[k, l])) *
-                Fraction(2) ** (-int(we[l, k] if axis == 0 else we[k, l])) for l in range(W.shape[axis])]
-        out.append(max(vals))
-    return out
-
-
-def test_max_scaled_exact_fallback_and_fast_path():
-    """The accu maxima max_j Wbar_ij 2**-v_j (rows) and max_i Wbar_ij 2**-u_i
-    (columns) against brute force over exact Fractions: once on ordinary
-    values (float path) and once where the scaled values are subnormal or
-    would not round-trip in float64 (exact Fraction path)."""
-    rng = np.random.default_rng(12)
-    W = rng.integers(0, 2**31, size=(6, 5)).astype(np.int64)
-    u = rng.integers(-40, 40, size=6)
-    v = rng.integers(-40, 40, size=5)
-    cases = [(W, u, v)]
-    # subnormal-range exponents: 2**-1070 Wbar is subnormal; 2**-1060 Wbar would round
-    W2 = W.copy()
-    W2[2, :] = [3, 2**30 + 1, 7, 0, 2**31 - 1]
-    u2 = u.copy()
-    u2[2] = 1070
-    v2 = v.copy()
-    v2[3] = 1060
-    cases.append((W2, u2, v2))
-    # two candidates that float64 cannot tell apart: (2**30 + 1) 2**-1080 rounds to 2**-1050
-    W3 = np.zeros((3, 2), dtype=np.int64)
-    W3[0, 0], W3[1, 0], W3[2, 1] = 2**30, 2**30 + 1, 5
-    cases.append((W3, np.array([1080, 1080, 0]), np.array([1080, 1080])))
-    for Wc, uc, vc in cases:
-        for axis, wexp in ((1, vc[None, :]), (0, uc[:, None])):
-            idx = oz._max_scaled(Wc, wexp, axis)
-            want = _max_scaled_brute(Wc, wexp, axis)
-            we = np.broadcast_to(wexp, Wc.shape)
-            for k, l in enumerate(idx):
-                i, j = (k, int(l)) if axis == 1 else (int(l), k)
-                assert Fraction(int(Wc[i, j])) * Fraction(2) ** (-int(we[i, j])) == want[k]
-
-
 def test_accu_exponents_subnormal_row_and_huge_column():
-    """accu mode with a row of |a| ~ 1e-310 (u_i ~ 1030, so its scaled bound
-    products are subnormal) and a column of B near 1e300 (v_j ~ -990): alpha
-    and beta against exact brute-force maxima of Wbar_ij 2**-(u_i + v_j)."""
+    """accu mode with a row of |a| ~ 1e-310 (u_i ~ 1030) and a column of B near
+    1e300 (v_j ~ -990): alpha_i = u_i + max {a : 4**a R_i <= L} with R_i the
+    brute-force row maximum of Wbar, beta_j likewise, and the scaled bound
+    2**(alpha_i + beta_j) (|A||B|)_ij <= L on exact values."""
     A, B = make_matrices(5, 12, 4, 1.0, 44)
     A[1, :] *= 1e-310
     B[:, 2] *= 1e300
@@ -383,11 +342,44 @@ def test_accu_exponents_subnormal_row_and_huge_column():
     al, be, Abar, Bbar, u, v, W = oz.accu_exponents(A, B, L)
     assert u[1] > 1000 and v[2] < -900
     for i in range(5):
-        Ui = max(Fraction(int(W[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) for j in range(4))
-        assert int(al[i]) == (_max_pow4_brute(Ui, L) if Ui else 0)
+        Ri = max(int(W[i, j]) for j in range(4))
+        assert int(al[i]) == (int(u[i]) + _max_pow4_brute(Fraction(Ri), L) if Ri else 0)
     for j in range(4):
-        Vj = max(Fraction(int(W[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) for i in range(5))
-        assert int(be[j]) == (_max_pow4_brute(Vj, L) if Vj else 0)
+        Kj = max(int(W[i, j]) for i in range(5))
+        assert int(be[j]) == (int(v[j]) + _max_pow4_brute(Fraction(Kj), L) if Kj else 0)
+    for i in range(5):
+        for j in range(4):
+            exact = sum(abs(Fraction(float(A[i, l])) * Fraction(float(B[l, j]))) for l in range(12))
+            assert Fraction(2) ** (int(al[i]) + int(be[j])) * exact <= L
+
+
+def test_accu_rows_and_columns_keep_their_own_scale():
+    """Rows of A at 2**+-1000 and columns of B at 2**30 .. 2**-100: no row's or
+    column's exponent is set by another's magnitude, so every output keeps
+    its significant bits.  The oracle's C at every entry against the exact
+    product (Fractions): relative error below 2**-40, exact zeros where the
+    product is zero, and +-inf exactly where the product passes the double
+    range."""
+    A, B = make_matrices(8, 24, 7, 0.5, 12)
+    A[0, :] *= 2.0**1000
+    A[1, :] *= -(2.0**1000)
+    A[2, :] *= 2.0**-1000
+    B[:, 0] *= 2.0**30
+    B[:, 1] *= 2.0**-70
+    B[:, 2] *= 2.0**-100
+    C = oz.oracle_dgemm(A, B, 14, "accu")["C"]
+    big = Fraction(2) ** 1024
+    for i in range(8):
+        for j in range(7):
+            ex = sum(Fraction(float(A[i, l])) * Fraction(float(B[l, j])) for l in range(24))
+            if abs(ex) >= big:
+                assert np.isinf(C[i, j]) and (C[i, j] > 0) == (ex > 0)
+            elif ex == 0:
+                assert C[i, j] == 0
+            elif abs(ex) >= Fraction(2) ** -1022:  # normal results: relative error
+                assert abs(Fraction(float(C[i, j])) - ex) <= abs(ex) * Fraction(2) ** -40, (i, j)
+            else:  # subnormal range: within a few units of 2**-1074
+                assert abs(Fraction(float(C[i, j])) - ex) <= Fraction(2) ** -1070, (i, j)
 
 
 def test_accu_bound_dominates_abs_product():
@@ -534,10 +526,21 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     assert fails(big)
     monkeypatch.setattr(oz, "np", np)
 
-    # the accu maxima taken in float64 alone (no exact fallback)
-    orig_ms = oz._max_scaled
-    monkeypatch.setattr(oz, "_max_scaled", lambda W, we, axis: np.argmax(
-        np.ldexp(np.asarray(W, dtype=np.float64), -we), axis=axis))
-    assert fails(test_max_scaled_exact_fallback_and_fast_path)
-    monkeypatch.setattr(oz, "_max_scaled", orig_ms)
-    assert not fails(test_max_scaled_exact_fallback_and_fast_path)
+    # accu exponents from the bound's maxima in the original scale, split
+    # evenly between the row and the column (an earlier reading): a huge row
+    # then sets every column's beta and the other rows lose their bits
+    orig_accu = oz.accu_exponents
+
+    def original_scale_split(A, B, L):
+        al, be, Abar, Bbar, u, v, W = orig_accu(A, B, L)
+        Wf = [[Fraction(int(W[i, j])) * Fraction(2) ** (-int(u[i]) - int(v[j])) for j in range(W.shape[1])]
+              for i in range(W.shape[0])]
+        al2 = np.array([oz.max_pow4_exponent(max(row), L) if max(row) else 0 for row in Wf])
+        be2 = np.array([oz.max_pow4_exponent(max(col), L) if max(col) else 0 for col in zip(*Wf)])
+        return al2, be2, Abar, Bbar, u, v, W
+
+    monkeypatch.setattr(oz, "accu_exponents", original_scale_split)
+    assert fails(test_accu_rows_and_columns_keep_their_own_scale)
+    assert fails(test_exponents_scale_equivariant)
+    monkeypatch.setattr(oz, "accu_exponents", orig_accu)
+    assert not fails(test_accu_rows_and_columns_keep_their_own_scale)

@@ -96,13 +96,18 @@ def test_fast_b_side_register_chunks_and_fallback(oz2, q):
     _full_check(oz2, A, B, 14, "fast")
 
 
-def test_fast_b_side_unaligned_columns(oz2):
-    # odd ldb: most columns of B start off a 16-byte boundary (scalar loads)
-    A, B = make_matrices(48, 777, 33, 2.0, 11)
-    bigB = torch.zeros((33, 781), dtype=torch.float64).t()  # (781, 33), strides (1, 781)
-    bigB[:777] = torch.from_numpy(B)
-    dB = bigB.cuda()[:777]
-    assert dB.stride() == (1, 781)
+@pytest.mark.parametrize("q", [777, 3001, 8191])
+def test_fast_b_side_unaligned_columns(oz2, q):
+    """odd q and odd ldb = q + 4: the odd columns of B start 8 bytes past a
+    16-byte boundary.  q = 777: the one-read kernel's scalar loads; q = 3001
+    and 8191: the bulk-copy statistics kernel, whose copy covers each
+    column's aligned middle, with the element before it (odd columns) or the
+    one after it (even columns) read separately."""
+    A, B = make_matrices(48, q, 33, 2.0, 11)
+    bigB = torch.zeros((33, q + 4), dtype=torch.float64).t()  # (q + 4, 33), strides (1, q + 4)
+    bigB[:q] = torch.from_numpy(B)
+    dB = bigB.cuda()[:q]
+    assert dB.stride() == (1, q + 4)
     got = oz2.dgemm_debug(_dev(A), dB, 14, "fast", want_p=False)
     ref = oracle.oracle_dgemm(A, B, 14, "fast")
     np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref["beta"])
@@ -168,6 +173,31 @@ def test_special_values(oz2, mode):
     B[:, 9] *= 2.0**-1000
     A[8, ::2] = -0.0
     _full_check(oz2, A, B, 14, mode)
+
+
+@pytest.mark.parametrize("mode", ["fast", "accu"])
+def test_outputs_past_the_double_range(oz2, mode):
+    """Outputs that overflow to +-inf, that sit next to the overflow threshold,
+    that are subnormal and that underflow: the CRT's exact rounding path
+    (results outside the normal range) against the oracle's one correct
+    rounding with overflow to +-inf and gradual underflow."""
+    A, B = make_matrices(64, 100, 40, 0.5, 12)
+    A[0, :] *= 2.0**1000
+    A[1, :] *= -(2.0**1000)
+    A[2, :] *= 2.0**-1000
+    A[3, :] *= -(2.0**-1000)
+    B[:, 0] *= 2.0**30    # rows 0, 1: far past the largest double
+    B[:, 1] *= 2.0**20    # next to it
+    B[:, 2] *= 2.0**22
+    B[:, 3] *= 2.0**-70   # rows 2, 3: subnormal
+    B[:, 4] *= 2.0**-100  # underflow toward zero
+    B[:, 5] *= 2.0**-52
+    got, ref = _full_check(oz2, A, B, 14, mode)
+    C = ref["C"]  # (the GPU's C equals it within 2 ulp, checked above)
+    assert C[0, 0] == np.inf and C[1, 0] == -np.inf
+    assert np.isfinite(C[0, 2]) and abs(C[0, 2]) > 1e307  # next to the largest double
+    sub = np.abs(C[2:4, 3:6])
+    assert np.any((sub > 0) & (sub < np.finfo(np.float64).tiny))
 
 
 def test_wide_range_accu_general_residue_path(oz2):
