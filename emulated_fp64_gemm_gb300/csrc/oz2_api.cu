@@ -607,7 +607,7 @@ oz2_status run_pipeline(int64_t p, int64_t q, int64_t r, const double* A, int64_
     // are consumed by the bound GEMM before the residue kernels overwrite them
     uint16_t* Abar = planesA;
     uint16_t* Bbar = planesB;
-    OZ2_CU(launch_bound_quant(sa, qp, amaxA, amaxB, u, v, Abar, Bbar, st));
+    OZ2_CU(launch_bound_quant(sa, qp, amaxA, amaxB, u, v, Abar, Bbar, ds->err, st));
     if (ev) OZ2_CU(cudaEventRecord(ev[1], st));
     OZ2_CU(cudaMemsetAsync(rowkey, 0, p * 8, st));
     OZ2_CU(cudaMemsetAsync(colkey, 0, r * 8, st));

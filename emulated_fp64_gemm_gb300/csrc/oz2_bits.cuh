@@ -97,5 +97,15 @@ __device__ __forceinline__ uint32_t pack_fp16_pair(uint32_t v0, uint32_t v1, __h
   return *reinterpret_cast<uint32_t*>(&hv);
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from global memory to this CTA's
+// shared memory, both addresses 16-byte aligned, counted on an mbarrier.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+constexpr uint64_t kStatsWaitNs = 2ull * 1000 * 1000 * 1000;  // 2 s: a 64 KB copy takes microseconds
+
 }  // namespace
 }  // namespace oz2

@@ -98,7 +98,7 @@ cudaError_t launch_fast_exponents_cols(const ScaleArgs& a, const BoundConsts& bc
 // accu mode, first half: amax, quantised bound planes Abar [p][qp], Bbar [r][qp] (fp16),
 // and the quantisation exponents u[p], v[r].
 cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,
-                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar,
+                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar, int* err,
                                cudaStream_t st);
 // accu mode, second half: exponents from the row / column max keys.
 cudaError_t launch_accu_exponents(int64_t p, int64_t r, const BoundConsts& bc,

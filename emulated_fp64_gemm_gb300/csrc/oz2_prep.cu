@@ -308,6 +308,102 @@ __global__ void __launch_bounds__(256, 2) fused_cols_bound_kernel(const double* 
   }
 }
 
+// Accu mode, B side in one read of B for 2048 < q <= 8192: one block per
+// column.  The column (contiguous in column-major B) comes into shared memory
+// by one bulk copy of its 16-byte aligned middle, with the one element before
+// it (a column starting 8 bytes past a 16-byte boundary) and the one after it
+// stored beside it, so that column element l sits at word l + 2 - h.  The
+// column maximum gives v_j; each thread quantises a strided set of elements
+// (conflict-free shared-memory reads), and once every thread is done the fp16
+// row of Bbar is staged over the column and written with 16-byte stores.
+// Results are identical to amax_cols + bound_quant_cols.  A copy that has not
+// landed within kStatsWaitNs sets the timeout bit in *err, and the block
+// waits (bounded again) for it before leaving.
+constexpr int kBoundColsPerThread = 32;  // q <= 8192 = 256 threads x 32
+__global__ void __launch_bounds__(256, 3) bound_cols_bulk_kernel(const double* __restrict__ B, int64_t q,
+                                                                 int64_t ldb, int64_t qp,
+                                                                 uint64_t* __restrict__ amax,
+                                                                 int32_t* __restrict__ v_out,
+                                                                 uint16_t* __restrict__ Bbar, int* err) {
+  extern __shared__ __align__(16) uint8_t col_smem[];  // (q + 2) doubles; later qp halves
+  __shared__ uint64_t red[8];
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t j = blockIdx.x;
+  const double* col = B + j * ldb;
+  const int h = static_cast<int>((reinterpret_cast<uintptr_t>(col) >> 3) & 1);  // elements before the aligned middle
+  const int64_t nmid = ((q - h) / 2) * 2;                                         // elements in it (even)
+  double* xs = reinterpret_cast<double*>(col_smem);                              // element l at xs[l + 2 - h]
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bar), static_cast<uint32_t>(nmid * 8));
+    bulk_copy_g2s(smem_u32(col_smem + 16), col + h, static_cast<uint32_t>(nmid * 8), smem_u32(&bar));
+  }
+  const bool got = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, kStatsWaitNs);
+  if (__syncthreads_or(!got)) {
+    if (tid == 0) {
+      atomicOr(err, kErrTimeout);
+      mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, kStatsWaitNs);  // the copy still in flight
+    }
+    return;
+  }
+  if (tid == 0 && h) xs[1] = __ldg(col);                                       // the element before the middle
+  if (tid == 1 && h + nmid < q) xs[q + 1 - h] = __ldg(col + q - 1);            // the element after it
+  __syncthreads();
+  const double* xe = xs + 2 - h;  // xe[l] = column element l, 0 <= l < q
+  uint64_t m = 0;
+  for (int64_t l = tid; l < q; l += 256) {
+    const uint64_t b = static_cast<uint64_t>(__double_as_longlong(xe[l])) & ~(1ull << 63);
+    m = b > m ? b : m;
+  }
+  for (int o = 16; o; o >>= 1) {
+    const uint64_t y = __shfl_xor_sync(0xffffffffu, m, o);
+    m = y > m ? y : m;
+  }
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) m = red[w] > m ? red[w] : m;
+  const int v = quant_exp(m);
+  if (tid == 0) {
+    amax[j] = m;
+    v_out[j] = v;
+  }
+  // ceil(|b_l| 2^v) <= 127 for the elements l = tid + 256 k (0 past q)
+  uint32_t cq[kBoundColsPerThread];
+#pragma unroll
+  for (int k = 0; k < kBoundColsPerThread; ++k) {
+    const int64_t l = tid + 256ll * k;
+    uint32_t c = 0;
+    if (l < q) {
+      const Dec d = decode(xe[l]);
+      c = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
+    }
+    cq[k] = c;
+  }
+  __syncthreads();  // every element read: the fp16 row goes over the column
+  uint16_t* hs = reinterpret_cast<uint16_t*>(col_smem);
+#pragma unroll
+  for (int k = 0; k < kBoundColsPerThread; ++k) {
+    const int64_t l = tid + 256ll * k;
+    if (l < qp) {
+      // fp16 of an integer below 1024: bits 0x6400 + c encode 1024 + c; subtract 1024
+      const __half hv = __hsub(__ushort_as_half(static_cast<unsigned short>(0x6400u + cq[k])), __ushort_as_half(0x6400));
+      hs[l] = __half_as_ushort(hv);
+    }
+  }
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(col_smem);
+  uint4* dst = reinterpret_cast<uint4*>(Bbar + j * qp);
+  for (int64_t c16 = tid; c16 < qp / 8; c16 += 256) dst[c16] = src[c16];
+}
+
 // accu exponents ("Profiling Ozaki II" §2 and §5.1: the row and column
 // maxima of the bound output give the final scale exponents), with the
 // maxima taken in the quantised scale: for row i, R_i = max_j Wbar_ij (from
@@ -419,7 +515,7 @@ cudaError_t launch_fast_exponents(const ScaleArgs& a, const BoundConsts& bc, uin
 }
 
 cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, uint64_t* amaxB,
-                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar,
+                               int32_t* u, int32_t* v, uint16_t* Abar, uint16_t* Bbar, int* err,
                                cudaStream_t st) {
   const int sms = device_sms();
   cudaMemsetAsync(amaxA, 0, a.p * sizeof(uint64_t), st);
@@ -435,10 +531,15 @@ cudaError_t launch_bound_quant(const ScaleArgs& a, int64_t qp, uint64_t* amaxA, 
   const bool fused_b = cols_fused_fast_supported(a.q) && a.r <= 0x7FFFFFFF;
   if (fused_b) {
     const dim3 g(static_cast<unsigned>(a.r));
-    const int nch = static_cast<int>((qp + 2047) / 2048);
-    if (nch <= 1) fused_cols_bound_kernel<1><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
-    else if (nch <= 2) fused_cols_bound_kernel<2><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
-    else fused_cols_bound_kernel<4><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
+    if (qp <= 2048) {
+      fused_cols_bound_kernel<1><<<g, 256, 0, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar);
+    } else {
+      // (set on every launch: the attribute belongs to the current device)
+      const cudaError_t attr =
+          cudaFuncSetAttribute(bound_cols_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (8192 + 2) * 8);
+      if (attr != cudaSuccess) return attr;
+      bound_cols_bulk_kernel<<<g, 256, (a.q + 2) * 8, st>>>(a.B, a.q, a.ldb, qp, amaxB, v, Bbar, err);
+    }
   } else {
     amax_cols_kernel<<<dim3(static_cast<unsigned>(cb), splitB), 256, 0, st>>>(a.B, a.q, a.r, a.ldb, segB, amaxB);
   }

@@ -244,16 +244,6 @@ __global__ void __launch_bounds__(256, ResOcc<NW>::kMinBlocks) residue_cols_kern
   }
 }
 
-// Bulk copy of `bytes` (a multiple of 16) from global memory to this CTA's
-// shared memory, both addresses 16-byte aligned, counted on an mbarrier.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-constexpr uint64_t kStatsWaitNs = 2ull * 1000 * 1000 * 1000;  // 2 s: a 64 KB copy takes microseconds
-
 // Fast mode, statistics of B's columns in one read (2048 < q <= 8192): one
 // block per column.  The column (contiguous, column-major B) is brought into
 // shared memory by one bulk copy of its 16-byte aligned middle; the one

@@ -96,24 +96,26 @@ def test_fast_b_side_register_chunks_and_fallback(oz2, q):
     _full_check(oz2, A, B, 14, "fast")
 
 
+@pytest.mark.parametrize("mode", ["fast", "accu"])
 @pytest.mark.parametrize("q", [777, 3001, 8191])
-def test_fast_b_side_unaligned_columns(oz2, q):
+def test_b_side_unaligned_columns(oz2, q, mode):
     """odd q and odd ldb = q + 4: the odd columns of B start 8 bytes past a
-    16-byte boundary.  q = 777: the one-read kernel's scalar loads; q = 3001
-    and 8191: the bulk-copy statistics kernel, whose copy covers each
-    column's aligned middle, with the element before it (odd columns) or the
-    one after it (even columns) read separately."""
+    16-byte boundary.  q = 777: the one-read kernels' scalar loads; q = 3001
+    and 8191: the bulk-copy kernels (fast: statistics; accu: maximum and
+    quantised bound row), whose copy covers each column's aligned middle,
+    with the element before it (odd columns) or the one after it (even
+    columns) read separately."""
     A, B = make_matrices(48, q, 33, 2.0, 11)
     bigB = torch.zeros((33, q + 4), dtype=torch.float64).t()  # (q + 4, 33), strides (1, q + 4)
     bigB[:q] = torch.from_numpy(B)
     dB = bigB.cuda()[:q]
     assert dB.stride() == (1, q + 4)
-    got = oz2.dgemm_debug(_dev(A), dB, 14, "fast", want_p=False)
-    ref = oracle.oracle_dgemm(A, B, 14, "fast")
+    got = oz2.dgemm_debug(_dev(A), dB, 14, mode, want_p=False)
+    ref = oracle.oracle_dgemm(A, B, 14, mode)
     np.testing.assert_array_equal(got["beta"].cpu().numpy(), ref["beta"])
     np.testing.assert_array_equal(got["Bres"].cpu().numpy(), np.transpose(ref["Bres"], (0, 2, 1)))
     assert ulp_distance(got["C"].cpu().numpy(), ref["C"]) <= ULP_TOL
-    C2 = oz2.dgemm(_dev(A), dB, 14, "fast").cpu().numpy()
+    C2 = oz2.dgemm(_dev(A), dB, 14, mode).cpu().numpy()
     np.testing.assert_array_equal(C2, got["C"].cpu().numpy())
 
 
