@@ -178,19 +178,15 @@ __global__ void bound_quant_rows_kernel(const double* __restrict__ A, int64_t p,
   if (i >= p || l0 >= qp) return;
   const int u = quant_exp(amax[i]);
   if (l0 == 0) u_out[i] = u;
+  uint64_t b[8];  // the eight elements' bits, all loads in flight first (0 past q)
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    b[k] = (l0 + k < q) ? static_cast<uint64_t>(__double_as_longlong(__ldg(A + (l0 + k) * lda + i))) : 0ull;
   uint32_t w[4];
 #pragma unroll
   for (int k = 0; k < 8; k += 2) {
-    uint32_t c[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t l = l0 + k + h;
-      c[h] = 0;
-      if (l < q) {
-        const Dec d = decode(A[l * lda + i]);
-        c[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + u));
-      }
-    }
+    // ceil(|a| 2^u) <= 127: 32-bit operations on the top significand bits and a sticky bit
+    const uint32_t c[2] = {ceil_scaled_small(b[k], u), ceil_scaled_small(b[k + 1], u)};
     // fp16 of an integer c < 1024: bits 0x6400 + c encode 1024 + c; subtract 1024.
     const uint32_t word = (c[1] << 16 | c[0]) + 0x64006400u;
     __half2 hv = *reinterpret_cast<const __half2*>(&word);
@@ -210,19 +206,14 @@ __global__ void bound_quant_cols_kernel(const double* __restrict__ B, int64_t q,
   if (j >= r || l0 >= qp) return;
   const int v = quant_exp(amax[j]);
   if (l0 == 0) v_out[j] = v;
+  uint64_t b[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    b[k] = (l0 + k < q) ? static_cast<uint64_t>(__double_as_longlong(__ldg(B + j * ldb + l0 + k))) : 0ull;
   uint32_t w[4];
 #pragma unroll
   for (int k = 0; k < 8; k += 2) {
-    uint32_t c[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t l = l0 + k + h;
-      c[h] = 0;
-      if (l < q) {
-        const Dec d = decode(B[j * ldb + l]);
-        c[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
-      }
-    }
+    const uint32_t c[2] = {ceil_scaled_small(b[k], v), ceil_scaled_small(b[k + 1], v)};
     const uint32_t word = (c[1] << 16 | c[0]) + 0x64006400u;
     __half2 hv = *reinterpret_cast<const __half2*>(&word);
     hv = __hsub2(hv, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
@@ -291,12 +282,9 @@ __global__ void __launch_bounds__(256, 2) fused_cols_bound_kernel(const double* 
       uint32_t w[4];
 #pragma unroll
       for (int k = 0; k < 8; k += 2) {
-        uint32_t cq[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const Dec d = decode(x[c][k + h]);
-          cq[h] = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
-        }
+        const uint32_t cq[2] = {
+            ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(x[c][k])), v),
+            ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(x[c][k + 1])), v)};
         // fp16 of an integer below 1024: bits 0x6400 + c encode 1024 + c; subtract 1024
         const uint32_t word = (cq[1] << 16 | cq[0]) + 0x64006400u;
         __half2 hv = *reinterpret_cast<const __half2*>(&word);
@@ -380,12 +368,7 @@ __global__ void __launch_bounds__(256, 3) bound_cols_bulk_kernel(const double* _
 #pragma unroll
   for (int k = 0; k < kBoundColsPerThread; ++k) {
     const int64_t l = tid + 256ll * k;
-    uint32_t c = 0;
-    if (l < q) {
-      const Dec d = decode(xe[l]);
-      c = static_cast<uint32_t>(ceil_shift(d.mant, d.E + v));
-    }
-    cq[k] = c;
+    cq[k] = (l < q) ? ceil_scaled_small(static_cast<uint64_t>(__double_as_longlong(xe[l])), v) : 0u;
   }
   __syncthreads();  // every element read: the fp16 row goes over the column
   uint16_t* hs = reinterpret_cast<uint16_t*>(col_smem);
