@@ -31,12 +31,12 @@ __global__ void amax_rows_kernel(const double* __restrict__ A, int64_t p, int64_
   const int64_t l1 = min(q, l0 + cols_per_block);
   uint64_t m = 0;
   int64_t l = l0;
-  for (; l + 8 <= l1; l += 8) {  // eight loads in flight per thread
-    uint64_t b[8];
+  for (; l + 16 <= l1; l += 16) {  // sixteen loads in flight per thread
+    uint64_t b[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(A + (l + k) * lda + i)));
+    for (int k = 0; k < 16; ++k) b[k] = static_cast<uint64_t>(__double_as_longlong(__ldg(A + (l + k) * lda + i)));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 16; ++k) {
       const uint64_t v = b[k] & ~(1ull << 63);
       m = v > m ? v : m;
     }
