@@ -48,7 +48,8 @@ def metric_name(workload) -> str:
     return (f"effective FP64 TFLOPS (2pqr/time), Ozaki-II p={w.p} q={w.q} r={w.r} s={w.s} {w.mode}; "
             "per-stage ms")
 UNIT = "TFLOP/s"
-# The pages' number for this metric and workload: GH200, fast-14, n=8192 (paper Table 3).
+# Published number for this metric and workload: GH200, fast-14, n=8192
+# ("Ozaki II supplement: INT8 range conditions and paper performance results", §3.1 Table 3).
 PAGES_BASELINE = {"n8192_s14_fast": 72.1}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "oz2_gemm_kernel_n8192_s14_fast.md")
@@ -297,7 +298,7 @@ def result_line(*, value, n_gpus, steps, warmup, ms_per_step, workload, extra):
             "tensor_path": "tcgen05.mma kind::f16 on integer residues, fp32 TMEM accumulation",
             "l2": "inputs larger than L2 (A+B = %.2f GB vs 129 MB)" % (8e-9 * (w.p * w.q + w.q * w.r)),
             "parallelism": f"replicas{n_gpus}",
-            "vs_baseline_ref": "GH200 fast-14 n=8192, 72.1 TFLOPS (paper Table 3)" if base else None,
+            "vs_baseline_ref": "GH200 fast-14 n=8192, 72.1 TFLOPS (Ozaki II supplement, §3.1 Table 3)" if base else None,
         },
     }
     out.update(extra)
